@@ -1,0 +1,182 @@
+/*
+ * plsh.h -- C ABI of the Positional LSH approximate-ALiBi attention library
+ * for GB300 (sm_103a).
+ *
+ * The method ("Positional LSH: Binary Block Matrix Approximation for
+ * Attention with Linear Biases", Wolfson & Wagner; technical summary):
+ *   Methodology 1   L*_ij = exp(-|i-j|/sigma) is a Laplacian kernel on token
+ *                   positions.  A random-binning hash of the integer positions
+ *                   splits 0..n-1 into contiguous bins; M(h) is 1 where i and
+ *                   j share a bin, and L* = E_h[M(h)].
+ *   Methodology 2   (Theorem 2.1) the mean M~ of s i.i.d. masks approximates
+ *                   L*; bin widths follow a Gamma law.
+ *   Methodology 3   (Theorem 2.2) ALiBi attention becomes s sets of short
+ *                   block attentions with no positional bias:
+ *                     T~ = D~^-1 (M~ o exp(QK^T/sqrt(d))) V,
+ *                   numerator and row sums both averaged over the s masks.
+ *
+ * Conventions shared by every call:
+ *   - Tensors are [B, H, n, d] contiguous row-major, on the CUDA device
+ *     that is current when the call is made, 16-byte aligned.  Query head h
+ *     reads KV head h / (Hq / Hkv) (contiguous GQA groups).
+ *   - The caller owns Q, K, V and O.  The library owns plsh_bins handles and
+ *     its per-device work-queue state.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call
+ *     is asynchronous on it except where a comment says it synchronises.
+ *   - Arguments are validated before anything is launched; on a validation
+ *     error nothing is written and the status says why (plsh_last_error()
+ *     holds a message for the calling thread).  No call aborts or prints.
+ */
+#ifndef PLSH_H_
+#define PLSH_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PLSH_OK = 0,
+  PLSH_ERR_INVALID = 1,      /* bad argument: shape, dtype, range, pointer  */
+  PLSH_ERR_CUDA = 2,         /* a CUDA runtime/driver call failed           */
+  PLSH_ERR_NOMEM = 3,        /* device or host allocation failed            */
+  PLSH_ERR_TIMEOUT = 4,      /* a device-side bounded wait ran out          */
+  PLSH_ERR_UNSUPPORTED = 5   /* valid request this build does not serve     */
+} plsh_status;
+
+typedef enum { PLSH_F32 = 0, PLSH_BF16 = 1 } plsh_dtype;
+
+/* A device tensor [B, H, n, d], contiguous, element type `dtype`.
+ * `data` is a device pointer the caller owns. */
+typedef struct {
+  void* data;
+  int32_t dtype;   /* plsh_dtype */
+  int64_t B, H, n, d;
+} plsh_tensor;
+
+/* Opaque set of s bin partitions per head (one per hash), resident on one
+ * device.  Owns its device memory; reusable by any number of attention
+ * calls (the same draws serve every batch element and layer). */
+typedef struct plsh_bins plsh_bins;
+
+/*
+ * plsh_sample_bins -- draw s random-binning hashes per head and build their
+ * bins on the device (Methodology 1-2).
+ *
+ * For head h and sample t the counter-based generator Philox4x32-10 (key =
+ * seed, counter = (t, h, 0, 0)) gives U0, U1, U2 = (x + 0.5) 2^-32; the width
+ * is w = sigma_h (-ln U0 - ln U1) ~ Gamma(shape 2, scale sigma_h) and the
+ * offset u = w U2 ~ U(0, w).  Bin starts are 0 and ceil(u + k w) for
+ * k = 0, 1, ... below n (every position its own bin when w < 1).  The
+ * arithmetic is fp64 with each operation rounded separately, so the starts
+ * agree bit for bit with any other implementation of the same recipe.
+ *
+ *   n        sequence length, 1 <= n < 2^31
+ *   sigma_h  host array [H], each finite and > 0 (sigma = 1 / ALiBi slope)
+ *   H        number of query heads, >= 1
+ *   s        hashes per head, 1 <= s <= 64
+ *   seed     64-bit generator key
+ *   out      receives a new handle (free with plsh_bins_free)
+ * Allocates device memory (synchronous allocation), then launches the
+ * sampler on `stream`.  On error *out is left unchanged.
+ */
+plsh_status plsh_sample_bins(int64_t n, const double* sigma_h, int32_t H,
+                             int32_t s, uint64_t seed, void* stream,
+                             plsh_bins** out);
+
+/*
+ * plsh_bins_resample -- redraw an existing handle in place with new sigma_h
+ * and seed (same n, H, s).  Allocates nothing; fully asynchronous.  The
+ * previous contents must no longer be in use by work queued on other
+ * streams.
+ */
+plsh_status plsh_bins_resample(plsh_bins* bins, const double* sigma_h,
+                               uint64_t seed, void* stream);
+
+/*
+ * plsh_bins_from_host -- build a handle from explicit bin boundaries (for
+ * deterministic variants such as fixed blocks, or draws made elsewhere).
+ *   offsets  host int64 [H*s + 1]; hash (h, t) owns
+ *            starts[offsets[h*s+t] .. offsets[h*s+t+1])
+ *   starts   host int32; each hash's list begins with 0, strictly increases
+ *            and ends with the terminal n
+ * Validated on the host; synchronous upload.
+ */
+plsh_status plsh_bins_from_host(int64_t n, int32_t H, int32_t s,
+                                const int64_t* offsets, const int32_t* starts,
+                                void* stream, plsh_bins** out);
+
+/* Shape of a handle.  n_entries (bins + terminals over all hashes) needs the
+ * device contents: this call synchronises `stream` when n_entries != NULL. */
+plsh_status plsh_bins_info(const plsh_bins* bins, int64_t* n, int32_t* H,
+                           int32_t* s, int64_t* n_entries, void* stream);
+
+/*
+ * plsh_bins_to_host -- copy the bin boundaries back in the plsh_bins_from_host
+ * layout.  offsets [H*s+1]; starts must hold `cap` entries (query the size
+ * with plsh_bins_info).  Synchronises `stream`.
+ */
+plsh_status plsh_bins_to_host(const plsh_bins* bins, int64_t* offsets,
+                              int32_t* starts, int64_t cap, void* stream);
+
+/* Draws (w, u) of every (h, t), host arrays [H*s] (either may be NULL).
+ * Synchronises `stream`. */
+plsh_status plsh_bins_draws(const plsh_bins* bins, double* w, double* u,
+                            void* stream);
+
+/* Frees the handle's device memory (synchronises the device first). */
+void plsh_bins_free(plsh_bins* bins);
+
+/*
+ * plsh_alibi_attn -- approximate ALiBi attention T~ (Methodology 3).
+ *
+ * For each batch b, query head h and row i, with J_t(i) the bin of i under
+ * hash t of head h (clipped to j <= i when causal):
+ *   O_i = sum_t sum_{j in J_t(i)} e^{S_ij} v_j / sum_t sum_{j in J_t(i)} e^{S_ij},
+ *   S_ij = q_i . k_j / sqrt(d).
+ * Computed as sum_j c_ij e^{S_ij} v_j / sum_j c_ij e^{S_ij}, with c_ij the
+ * number of hashes that put i and j in one bin.
+ *
+ *   Q [B,Hq,n,d]; K, V [B,Hkv,n,d]; O [B,Hq,n,d], all the same dtype
+ *   (PLSH_BF16: tcgen05 tensor-core path, d = 128; PLSH_F32 or d = 64: CUDA
+ *   core path; fp32 accumulation and softmax in both).  Hq % Hkv == 0,
+ *   bins->n == n, bins->H == Hq, d in {64, 128}.
+ *   causal   non-zero: keys j <= i only.
+ * Asynchronous on `stream`.  A device-side wait that runs out (a bug, never
+ * expected) is reported by the next plsh_stream_status().
+ */
+plsh_status plsh_alibi_attn(const plsh_tensor* Q, const plsh_tensor* K,
+                            const plsh_tensor* V, const plsh_bins* bins,
+                            int32_t causal, plsh_tensor* O, void* stream);
+
+/*
+ * plsh_alibi_exact -- exact ALiBi attention T* (the dense comparator, Problem
+ * statement: O(n^2) in the bias matrix):
+ *   O_i = sum_j e^{S_ij - |i-j|/sigma_h} v_j / sum_j e^{S_ij - |i-j|/sigma_h}
+ * over all j (j <= i when causal).  sigma_h: host array [Hq], finite, > 0.
+ * Same tensor rules as plsh_alibi_attn.
+ */
+plsh_status plsh_alibi_exact(const plsh_tensor* Q, const plsh_tensor* K,
+                             const plsh_tensor* V, const double* sigma_h,
+                             int32_t causal, plsh_tensor* O, void* stream);
+
+/* Synchronises `stream`, then reports CUDA errors and the library's device
+ * error flag (PLSH_ERR_TIMEOUT when a bounded device wait ran out), clearing
+ * the flag. */
+plsh_status plsh_stream_status(void* stream);
+
+/* Debug knob: limit in nanoseconds of every device-side wait launched after
+ * this call on the current device (0 restores the default of 2 s). */
+plsh_status plsh_set_wait_limit_ns(uint64_t ns);
+
+const char* plsh_status_string(plsh_status status);
+
+/* Message of the last error raised on the calling thread ("" if none). */
+const char* plsh_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PLSH_H_ */

@@ -1,0 +1,476 @@
+// C ABI entry points (include/plsh.h): validation, handles, dispatch.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <algorithm>
+#include <mutex>
+#include <numeric>
+#include <string>
+#include <vector>
+
+#include "plsh_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+plsh_status fail(plsh_status st, const std::string& msg) {
+  g_last_error = msg;
+  return st;
+}
+
+plsh_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(PLSH_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+#define PLSH_TRY_CUDA(expr, what)                      \
+  do {                                                 \
+    cudaError_t e_ = (expr);                           \
+    if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+  } while (0)
+
+constexpr int kMaxDevices = 64;
+std::mutex g_ctx_mu;
+plsh::DeviceCtx g_ctx[kMaxDevices];
+
+bool fault_oom() {
+  const char* f = getenv("PLSH_FAULT");
+  return f != nullptr && strcmp(f, "oom") == 0;
+}
+
+plsh_status dev_alloc(void** p, size_t bytes, const char* what) {
+  if (fault_oom()) return fail(PLSH_ERR_NOMEM, std::string(what) + ": injected allocation failure");
+  cudaError_t e = cudaMalloc(p, bytes == 0 ? 16 : bytes);
+  if (e == cudaErrorMemoryAllocation) {
+    cudaGetLastError();
+    return fail(PLSH_ERR_NOMEM, std::string(what) + ": out of device memory");
+  }
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  return PLSH_OK;
+}
+
+// Context of the current device, created on first use.
+plsh_status current_ctx(plsh::DeviceCtx** out) {
+  int dev = -1;
+  PLSH_TRY_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(PLSH_ERR_UNSUPPORTED, "device index out of range");
+  std::lock_guard<std::mutex> lk(g_ctx_mu);
+  plsh::DeviceCtx& c = g_ctx[dev];
+  if (c.device < 0) {
+    int sms = 0;
+    PLSH_TRY_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev),
+                  "cudaDeviceGetAttribute");
+    int* err = nullptr;
+    int* queue = nullptr;
+    plsh_status st = dev_alloc((void**)&err, sizeof(int), "error flag");
+    if (st != PLSH_OK) return st;
+    st = dev_alloc((void**)&queue, sizeof(int) * 2 * plsh::kQueueSlots, "work queues");
+    if (st != PLSH_OK) {
+      cudaFree(err);
+      return st;
+    }
+    PLSH_TRY_CUDA(cudaMemset(err, 0, sizeof(int)), "cudaMemset");
+    PLSH_TRY_CUDA(cudaMemset(queue, 0, sizeof(int) * 2 * plsh::kQueueSlots), "cudaMemset");
+    PLSH_TRY_CUDA(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
+    c.num_sms = sms;
+    c.d_err = err;
+    c.d_queue = queue;
+    c.device = dev;
+  }
+  *out = &c;
+  return PLSH_OK;
+}
+
+plsh_status check_sigma(const double* sigma, int32_t H) {
+  if (sigma == nullptr) return fail(PLSH_ERR_INVALID, "sigma_h is NULL");
+  for (int32_t h = 0; h < H; ++h) {
+    const double v = sigma[h];
+    if (!(v > 0.0) || !(v <= 1e15) || !isfinite(v))
+      return fail(PLSH_ERR_INVALID, "sigma_h[" + std::to_string(h) +
+                                        "] must be finite and in (0, 1e15]");
+  }
+  return PLSH_OK;
+}
+
+void order_heads(plsh_bins* b) {
+  b->head_order.resize(b->H);
+  std::iota(b->head_order.begin(), b->head_order.end(), 0);
+  std::stable_sort(b->head_order.begin(), b->head_order.end(),
+                   [&](int x, int y) { return b->sigma_host[x] > b->sigma_host[y]; });
+}
+
+void free_bins(plsh_bins* b) {
+  if (!b) return;
+  int prev = -1;
+  cudaGetDevice(&prev);
+  cudaSetDevice(b->device);
+  cudaDeviceSynchronize();
+  cudaFree(b->d_sigma);
+  cudaFree(b->d_w);
+  cudaFree(b->d_u);
+  cudaFree(b->d_rec);
+  cudaFree(b->d_head_order);
+  if (prev >= 0) cudaSetDevice(prev);
+  delete b;
+}
+
+plsh_status new_bins(int64_t n, int32_t H, int32_t s, plsh_bins** out) {
+  int dev = -1;
+  PLSH_TRY_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  plsh_bins* b = new (std::nothrow) plsh_bins();
+  if (!b) return fail(PLSH_ERR_NOMEM, "host allocation");
+  b->device = dev;
+  b->n = n;
+  b->H = H;
+  b->s = s;
+  b->W = (n + 31) / 32;
+  const size_t HS = (size_t)H * s;
+  plsh_status st;
+  if ((st = dev_alloc((void**)&b->d_sigma, sizeof(double) * H, "sigma")) != PLSH_OK ||
+      (st = dev_alloc((void**)&b->d_w, sizeof(double) * HS, "draws")) != PLSH_OK ||
+      (st = dev_alloc((void**)&b->d_u, sizeof(double) * HS, "draws")) != PLSH_OK ||
+      (st = dev_alloc((void**)&b->d_rec, sizeof(plsh::BinRecord) * HS * b->W, "bin records")) != PLSH_OK ||
+      (st = dev_alloc((void**)&b->d_head_order, sizeof(int32_t) * H, "head order")) != PLSH_OK) {
+    free_bins(b);
+    return st;
+  }
+  *out = b;
+  return PLSH_OK;
+}
+
+plsh_status check_bins_device(const plsh_bins* b) {
+  int dev = -1;
+  PLSH_TRY_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  if (dev != b->device) return fail(PLSH_ERR_INVALID, "bins handle lives on another device");
+  return PLSH_OK;
+}
+
+plsh_status resample(plsh_bins* b, const double* sigma, uint64_t seed, cudaStream_t st) {
+  b->sigma_host.assign(sigma, sigma + b->H);
+  order_heads(b);
+  PLSH_TRY_CUDA(cudaMemcpyAsync(b->d_sigma, sigma, sizeof(double) * b->H,
+                                cudaMemcpyHostToDevice, st), "copy sigma");
+  PLSH_TRY_CUDA(cudaMemcpyAsync(b->d_head_order, b->head_order.data(),
+                                sizeof(int32_t) * b->H, cudaMemcpyHostToDevice, st),
+                "copy head order");
+  PLSH_TRY_CUDA(plsh::launch_sample(b, seed, st), "sampler launch");
+  return PLSH_OK;
+}
+
+// Host copy of the records -> (offsets, starts).  Synchronises `st`.
+plsh_status records_to_host(const plsh_bins* b, cudaStream_t st,
+                            std::vector<int64_t>* offsets, std::vector<int32_t>* starts) {
+  const size_t HS = (size_t)b->H * b->s;
+  std::vector<plsh::BinRecord> rec(HS * b->W);
+  PLSH_TRY_CUDA(cudaMemcpyAsync(rec.data(), b->d_rec, sizeof(plsh::BinRecord) * rec.size(),
+                                cudaMemcpyDeviceToHost, st), "copy records");
+  PLSH_TRY_CUDA(cudaStreamSynchronize(st), "cudaStreamSynchronize");
+  offsets->assign(HS + 1, 0);
+  starts->clear();
+  for (size_t hs = 0; hs < HS; ++hs) {
+    (*offsets)[hs] = (int64_t)starts->size();
+    for (int64_t w = 0; w < b->W; ++w) {
+      uint32_t bits = rec[hs * b->W + w].bits;
+      while (bits) {
+        const int r = __builtin_ctz(bits);
+        starts->push_back((int32_t)(w * 32 + r));
+        bits &= bits - 1;
+      }
+    }
+    starts->push_back((int32_t)b->n);
+  }
+  (*offsets)[HS] = (int64_t)starts->size();
+  return PLSH_OK;
+}
+
+plsh_status check_tensor(const plsh_tensor* t, const char* name) {
+  if (t == nullptr) return fail(PLSH_ERR_INVALID, std::string(name) + " is NULL");
+  if (t->data == nullptr) return fail(PLSH_ERR_INVALID, std::string(name) + "->data is NULL");
+  if (((uintptr_t)t->data & 15u) != 0)
+    return fail(PLSH_ERR_INVALID, std::string(name) + "->data must be 16-byte aligned");
+  if (t->dtype != PLSH_F32 && t->dtype != PLSH_BF16)
+    return fail(PLSH_ERR_INVALID, std::string(name) + ": dtype must be PLSH_F32 or PLSH_BF16");
+  if (t->B < 1 || t->H < 1 || t->n < 1 || t->d < 1)
+    return fail(PLSH_ERR_INVALID, std::string(name) + ": every dimension must be >= 1");
+  return PLSH_OK;
+}
+
+plsh_status check_qkvo(const plsh_tensor* Q, const plsh_tensor* K, const plsh_tensor* V,
+                       const plsh_tensor* O) {
+  plsh_status st;
+  if ((st = check_tensor(Q, "Q")) != PLSH_OK || (st = check_tensor(K, "K")) != PLSH_OK ||
+      (st = check_tensor(V, "V")) != PLSH_OK || (st = check_tensor(O, "O")) != PLSH_OK)
+    return st;
+  if (K->dtype != Q->dtype || V->dtype != Q->dtype || O->dtype != Q->dtype)
+    return fail(PLSH_ERR_INVALID, "Q, K, V and O must share one dtype");
+  if (Q->d != 64 && Q->d != 128) return fail(PLSH_ERR_INVALID, "head dim d must be 64 or 128");
+  if (K->B != Q->B || K->n != Q->n || K->d != Q->d)
+    return fail(PLSH_ERR_INVALID, "K must be [B, Hkv, n, d] with Q's B, n, d");
+  if (V->B != K->B || V->H != K->H || V->n != K->n || V->d != K->d)
+    return fail(PLSH_ERR_INVALID, "V must have K's shape");
+  if (O->B != Q->B || O->H != Q->H || O->n != Q->n || O->d != Q->d)
+    return fail(PLSH_ERR_INVALID, "O must have Q's shape");
+  if (Q->H % K->H != 0) return fail(PLSH_ERR_INVALID, "Hq must be a multiple of Hkv");
+  if (Q->n >= ((int64_t)1 << 31)) return fail(PLSH_ERR_INVALID, "n must be < 2^31");
+  const int64_t tiles = Q->B * Q->H * ((Q->n + 127) / 128);
+  if (Q->B * Q->H >= ((int64_t)1 << 31) || tiles >= ((int64_t)1 << 31))
+    return fail(PLSH_ERR_INVALID, "B * Hq * ceil(n/128) must be < 2^31");
+  return PLSH_OK;
+}
+
+enum class Path { Auto, Simt, Tc };
+
+Path path_override() {
+  const char* p = getenv("PLSH_PATH");
+  if (p == nullptr) return Path::Auto;
+  if (strcmp(p, "simt") == 0) return Path::Simt;
+  if (strcmp(p, "tc") == 0) return Path::Tc;
+  return Path::Auto;
+}
+
+plsh_status run_attention(const plsh_tensor* Q, const plsh_tensor* K, const plsh_tensor* V,
+                          plsh_tensor* O, int causal, const plsh_bins* bins,
+                          const float* slopes, cudaStream_t st) {
+  plsh::DeviceCtx* ctx = nullptr;
+  plsh_status s0 = current_ctx(&ctx);
+  if (s0 != PLSH_OK) return s0;
+  plsh::AttnArgs a;
+  memset(&a, 0, sizeof a);
+  a.Q = Q->data;
+  a.K = K->data;
+  a.V = V->data;
+  a.O = O->data;
+  a.B = (int)Q->B;
+  a.Hq = (int)Q->H;
+  a.Hkv = (int)K->H;
+  a.n = (int)Q->n;
+  a.d = (int)Q->d;
+  a.causal = causal ? 1 : 0;
+  a.exact = bins == nullptr ? 1 : 0;
+  if (bins) {
+    a.rec = bins->d_rec;
+    a.s = bins->s;
+    a.W = bins->W;
+    a.head_order = bins->d_head_order;
+  }
+  a.err = ctx->d_err;
+  a.wait_ns = ctx->wait_ns;
+  {
+    std::lock_guard<std::mutex> lk(g_ctx_mu);
+    a.queue = ctx->d_queue + 2 * (ctx->slot_counter++ % plsh::kQueueSlots);
+  }
+  const bool tc_ok = Q->dtype == PLSH_BF16 && Q->d == 128 &&
+                     plsh::attn_tc_smem_bytes(a.s, a.causal, a.exact) <= 232448;
+  Path path = path_override();
+  if (path == Path::Auto) path = tc_ok ? Path::Tc : Path::Simt;
+  if (path == Path::Tc && !tc_ok)
+    return fail(PLSH_ERR_UNSUPPORTED, "tensor-core path needs bf16, d = 128 and s within "
+                                      "its shared-memory budget");
+  cudaError_t e = path == Path::Tc ? plsh::launch_attn_tc(a, slopes, ctx->num_sms, st)
+                                   : plsh::launch_attn_simt(a, slopes, Q->dtype, st);
+  if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+  return PLSH_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+plsh_status plsh_sample_bins(int64_t n, const double* sigma_h, int32_t H, int32_t s,
+                             uint64_t seed, void* stream, plsh_bins** out) {
+  if (out == nullptr) return fail(PLSH_ERR_INVALID, "out is NULL");
+  if (n < 1 || n >= ((int64_t)1 << 31)) return fail(PLSH_ERR_INVALID, "n must be in [1, 2^31)");
+  if (H < 1) return fail(PLSH_ERR_INVALID, "H must be >= 1");
+  if (s < 1 || s > plsh::kMaxS) return fail(PLSH_ERR_INVALID, "s must be in [1, 64]");
+  plsh_status st = check_sigma(sigma_h, H);
+  if (st != PLSH_OK) return st;
+  plsh::DeviceCtx* ctx = nullptr;
+  if ((st = current_ctx(&ctx)) != PLSH_OK) return st;
+  plsh_bins* b = nullptr;
+  if ((st = new_bins(n, H, s, &b)) != PLSH_OK) return st;
+  if ((st = resample(b, sigma_h, seed, (cudaStream_t)stream)) != PLSH_OK) {
+    free_bins(b);
+    return st;
+  }
+  *out = b;
+  return PLSH_OK;
+}
+
+plsh_status plsh_bins_resample(plsh_bins* bins, const double* sigma_h, uint64_t seed,
+                               void* stream) {
+  if (bins == nullptr) return fail(PLSH_ERR_INVALID, "bins is NULL");
+  plsh_status st = check_sigma(sigma_h, bins->H);
+  if (st != PLSH_OK) return st;
+  if ((st = check_bins_device(bins)) != PLSH_OK) return st;
+  return resample(bins, sigma_h, seed, (cudaStream_t)stream);
+}
+
+plsh_status plsh_bins_from_host(int64_t n, int32_t H, int32_t s, const int64_t* offsets,
+                                const int32_t* starts, void* stream, plsh_bins** out) {
+  if (out == nullptr || offsets == nullptr || starts == nullptr)
+    return fail(PLSH_ERR_INVALID, "NULL argument");
+  if (n < 1 || n >= ((int64_t)1 << 31)) return fail(PLSH_ERR_INVALID, "n must be in [1, 2^31)");
+  if (H < 1) return fail(PLSH_ERR_INVALID, "H must be >= 1");
+  if (s < 1 || s > plsh::kMaxS) return fail(PLSH_ERR_INVALID, "s must be in [1, 64]");
+  const int64_t HS = (int64_t)H * s;
+  if (offsets[0] != 0) return fail(PLSH_ERR_INVALID, "offsets[0] must be 0");
+  std::vector<double> sigma_est(H, 0.0);
+  for (int64_t hs = 0; hs < HS; ++hs) {
+    const int64_t o0 = offsets[hs], o1 = offsets[hs + 1];
+    if (o1 - o0 < 2 || o1 - o0 > n + 1)
+      return fail(PLSH_ERR_INVALID, "hash " + std::to_string(hs) + ": needs 2..n+1 entries");
+    if (starts[o0] != 0) return fail(PLSH_ERR_INVALID, "hash " + std::to_string(hs) + ": first start must be 0");
+    if (starts[o1 - 1] != n) return fail(PLSH_ERR_INVALID, "hash " + std::to_string(hs) + ": last entry must be n");
+    for (int64_t e = o0 + 1; e < o1; ++e)
+      if (starts[e] <= starts[e - 1])
+        return fail(PLSH_ERR_INVALID, "hash " + std::to_string(hs) + ": starts must strictly increase");
+    // mean bin width of a Gamma(2, sigma) draw is 2 sigma: a cost estimate
+    sigma_est[hs / s] += (double)n / (double)(o1 - o0 - 1) / (2.0 * s);
+  }
+  const int64_t total = offsets[HS];
+  plsh::DeviceCtx* ctx = nullptr;
+  plsh_status st = current_ctx(&ctx);
+  if (st != PLSH_OK) return st;
+  plsh_bins* b = nullptr;
+  if ((st = new_bins(n, H, s, &b)) != PLSH_OK) return st;
+  b->sigma_host = sigma_est;
+  order_heads(b);
+  cudaStream_t cs = (cudaStream_t)stream;
+  int32_t* d_starts = nullptr;
+  int64_t* d_off = nullptr;
+  if ((st = dev_alloc((void**)&d_starts, sizeof(int32_t) * total, "starts upload")) != PLSH_OK ||
+      (st = dev_alloc((void**)&d_off, sizeof(int64_t) * (HS + 1), "offsets upload")) != PLSH_OK) {
+    cudaFree(d_starts);
+    free_bins(b);
+    return st;
+  }
+  cudaError_t e = cudaMemcpyAsync(d_starts, starts, sizeof(int32_t) * total, cudaMemcpyHostToDevice, cs);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(d_off, offsets, sizeof(int64_t) * (HS + 1), cudaMemcpyHostToDevice, cs);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(b->d_head_order, b->head_order.data(), sizeof(int32_t) * H, cudaMemcpyHostToDevice, cs);
+  if (e == cudaSuccess) e = cudaMemsetAsync(b->d_w, 0, sizeof(double) * HS, cs);
+  if (e == cudaSuccess) e = cudaMemsetAsync(b->d_u, 0, sizeof(double) * HS, cs);
+  if (e == cudaSuccess) e = plsh::launch_bins_from_starts(b, d_starts, d_off, total, cs);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
+  cudaFree(d_starts);
+  cudaFree(d_off);
+  if (e != cudaSuccess) {
+    free_bins(b);
+    return cuda_fail(e, "bins upload");
+  }
+  *out = b;
+  return PLSH_OK;
+}
+
+plsh_status plsh_bins_info(const plsh_bins* bins, int64_t* n, int32_t* H, int32_t* s,
+                           int64_t* n_entries, void* stream) {
+  if (bins == nullptr) return fail(PLSH_ERR_INVALID, "bins is NULL");
+  if (n) *n = bins->n;
+  if (H) *H = bins->H;
+  if (s) *s = bins->s;
+  if (n_entries) {
+    plsh_status st = check_bins_device(bins);
+    if (st != PLSH_OK) return st;
+    std::vector<int64_t> off;
+    std::vector<int32_t> starts;
+    if ((st = records_to_host(bins, (cudaStream_t)stream, &off, &starts)) != PLSH_OK) return st;
+    *n_entries = (int64_t)starts.size();
+  }
+  return PLSH_OK;
+}
+
+plsh_status plsh_bins_to_host(const plsh_bins* bins, int64_t* offsets, int32_t* starts,
+                              int64_t cap, void* stream) {
+  if (bins == nullptr || offsets == nullptr || starts == nullptr)
+    return fail(PLSH_ERR_INVALID, "NULL argument");
+  plsh_status st = check_bins_device(bins);
+  if (st != PLSH_OK) return st;
+  std::vector<int64_t> off;
+  std::vector<int32_t> st_list;
+  if ((st = records_to_host(bins, (cudaStream_t)stream, &off, &st_list)) != PLSH_OK) return st;
+  if ((int64_t)st_list.size() > cap)
+    return fail(PLSH_ERR_INVALID, "starts buffer too small: need " + std::to_string(st_list.size()));
+  memcpy(offsets, off.data(), sizeof(int64_t) * off.size());
+  memcpy(starts, st_list.data(), sizeof(int32_t) * st_list.size());
+  return PLSH_OK;
+}
+
+plsh_status plsh_bins_draws(const plsh_bins* bins, double* w, double* u, void* stream) {
+  if (bins == nullptr) return fail(PLSH_ERR_INVALID, "bins is NULL");
+  plsh_status st = check_bins_device(bins);
+  if (st != PLSH_OK) return st;
+  const size_t HS = (size_t)bins->H * bins->s;
+  cudaStream_t cs = (cudaStream_t)stream;
+  if (w) PLSH_TRY_CUDA(cudaMemcpyAsync(w, bins->d_w, sizeof(double) * HS, cudaMemcpyDeviceToHost, cs), "copy w");
+  if (u) PLSH_TRY_CUDA(cudaMemcpyAsync(u, bins->d_u, sizeof(double) * HS, cudaMemcpyDeviceToHost, cs), "copy u");
+  PLSH_TRY_CUDA(cudaStreamSynchronize(cs), "cudaStreamSynchronize");
+  return PLSH_OK;
+}
+
+void plsh_bins_free(plsh_bins* bins) { free_bins(bins); }
+
+plsh_status plsh_alibi_attn(const plsh_tensor* Q, const plsh_tensor* K, const plsh_tensor* V,
+                            const plsh_bins* bins, int32_t causal, plsh_tensor* O,
+                            void* stream) {
+  plsh_status st = check_qkvo(Q, K, V, O);
+  if (st != PLSH_OK) return st;
+  if (bins == nullptr) return fail(PLSH_ERR_INVALID, "bins is NULL");
+  if (bins->n != Q->n) return fail(PLSH_ERR_INVALID, "bins were drawn for another n");
+  if (bins->H != Q->H) return fail(PLSH_ERR_INVALID, "bins were drawn for another number of heads");
+  if ((st = check_bins_device(bins)) != PLSH_OK) return st;
+  return run_attention(Q, K, V, O, causal, bins, nullptr, (cudaStream_t)stream);
+}
+
+plsh_status plsh_alibi_exact(const plsh_tensor* Q, const plsh_tensor* K, const plsh_tensor* V,
+                             const double* sigma_h, int32_t causal, plsh_tensor* O,
+                             void* stream) {
+  plsh_status st = check_qkvo(Q, K, V, O);
+  if (st != PLSH_OK) return st;
+  if (Q->H > plsh::kMaxExactHeads) return fail(PLSH_ERR_UNSUPPORTED, "exact path serves at most 512 heads");
+  if ((st = check_sigma(sigma_h, (int32_t)Q->H)) != PLSH_OK) return st;
+  std::vector<float> slopes(Q->H);
+  for (int64_t h = 0; h < Q->H; ++h) slopes[h] = (float)(1.4426950408889634 / sigma_h[h]);
+  return run_attention(Q, K, V, O, causal, nullptr, slopes.data(), (cudaStream_t)stream);
+}
+
+plsh_status plsh_stream_status(void* stream) {
+  plsh::DeviceCtx* ctx = nullptr;
+  plsh_status st = current_ctx(&ctx);
+  if (st != PLSH_OK) return st;
+  PLSH_TRY_CUDA(cudaStreamSynchronize((cudaStream_t)stream), "cudaStreamSynchronize");
+  PLSH_TRY_CUDA(cudaGetLastError(), "pending CUDA error");
+  int flag = 0;
+  PLSH_TRY_CUDA(cudaMemcpy(&flag, ctx->d_err, sizeof(int), cudaMemcpyDeviceToHost), "read error flag");
+  if (flag != 0) {
+    PLSH_TRY_CUDA(cudaMemset(ctx->d_err, 0, sizeof(int)), "clear error flag");
+    PLSH_TRY_CUDA(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
+    return fail(PLSH_ERR_TIMEOUT, "a device-side wait ran out of time");
+  }
+  return PLSH_OK;
+}
+
+plsh_status plsh_set_wait_limit_ns(uint64_t ns) {
+  plsh::DeviceCtx* ctx = nullptr;
+  plsh_status st = current_ctx(&ctx);
+  if (st != PLSH_OK) return st;
+  ctx->wait_ns = ns == 0 ? plsh::kDefaultWaitNs : ns;
+  return PLSH_OK;
+}
+
+const char* plsh_status_string(plsh_status status) {
+  switch (status) {
+    case PLSH_OK: return "ok";
+    case PLSH_ERR_INVALID: return "invalid argument";
+    case PLSH_ERR_CUDA: return "CUDA error";
+    case PLSH_ERR_NOMEM: return "out of memory";
+    case PLSH_ERR_TIMEOUT: return "device wait timed out";
+    case PLSH_ERR_UNSUPPORTED: return "unsupported";
+  }
+  return "unknown status";
+}
+
+const char* plsh_last_error(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

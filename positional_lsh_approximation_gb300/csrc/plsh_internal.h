@@ -1,0 +1,90 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "../../include/plsh.h"
+
+namespace plsh {
+
+// One record per (hash, 32-position word): which positions of the word open a
+// bin, the last bin start at or before the word's first position, and the
+// first bin start after the word (n when none).
+struct __align__(16) BinRecord {
+  uint32_t bits;
+  int32_t prev;
+  int32_t next;
+  int32_t pad;
+};
+
+constexpr int kMaxS = 64;
+constexpr int kMaxExactHeads = 512;
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+
+// Per-device library state.
+struct DeviceCtx {
+  int device = -1;
+  int num_sms = 0;
+  int* d_err = nullptr;        // device error flag (bit 0: wait timeout)
+  int* d_queue = nullptr;      // kQueueSlots x {next item, finished CTAs}
+  uint64_t slot_counter = 0;
+  uint64_t wait_ns = kDefaultWaitNs;
+};
+constexpr int kQueueSlots = 1024;
+
+}  // namespace plsh
+
+struct plsh_bins {
+  int device;
+  int64_t n;
+  int32_t H, s;
+  int64_t W;                      // words per hash = ceil(n / 32)
+  double* d_sigma = nullptr;      // [H]
+  double* d_w = nullptr;          // [H*s]
+  double* d_u = nullptr;          // [H*s]
+  plsh::BinRecord* d_rec = nullptr;  // [H*s][W]
+  int32_t* d_head_order = nullptr;   // [H]
+  std::vector<double> sigma_host;    // per-head scale (drawn or estimated)
+  std::vector<int32_t> head_order;   // heads by expected work, descending
+};
+
+namespace plsh {
+
+// sampler.cu
+cudaError_t launch_sample(plsh_bins* b, uint64_t seed, cudaStream_t st);
+cudaError_t launch_bins_from_starts(plsh_bins* b, const int32_t* d_starts,
+                                    const int64_t* d_offsets, int64_t total,
+                                    cudaStream_t st);
+
+// Arguments common to the attention kernels.
+struct AttnArgs {
+  const void* Q;
+  const void* K;
+  const void* V;
+  void* O;
+  int B, Hq, Hkv, n, d;
+  int causal;
+  int exact;                       // 1: exact ALiBi, 0: Positional LSH
+  const BinRecord* rec;            // [Hq*s][W] (approximate mode)
+  int s;
+  int64_t W;
+  const int32_t* head_order;       // [Hq] (approximate mode)
+  int* err;
+  int* queue;                      // {next item, finished CTAs}
+  uint64_t wait_ns;
+};
+
+// attn_simt.cu (CUDA cores, any dtype, d in {64, 128})
+// slopes_host: exact mode, [Hq] log2(e)/sigma_h (at most kMaxExactHeads)
+cudaError_t launch_attn_simt(const AttnArgs& a, const float* slopes_host,
+                             int dtype, cudaStream_t st);
+// attn_tc.cu (tcgen05 tensor cores, bf16, d = 128)
+cudaError_t launch_attn_tc(const AttnArgs& a, const float* slopes_host,
+                           int num_sms, cudaStream_t st);
+size_t attn_tc_smem_bytes(int s, int causal, int exact);
+
+}  // namespace plsh

@@ -1,0 +1,95 @@
+"""The C-ABI library builds, loads and exports every symbol of include/plsh.h;
+host-side validation rejects bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import positional_lsh_approximation_gb300 as plsh
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    with open(os.path.join(ROOT, "include", "plsh.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(plsh_[a-z_0-9]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    plsh.build()
+    return plsh.load()
+
+
+def test_header_declares_the_boundary():
+    syms = declared_symbols()
+    for name in ("plsh_sample_bins", "plsh_alibi_attn", "plsh_alibi_exact",
+                 "plsh_bins_from_host", "plsh_bins_to_host", "plsh_bins_free",
+                 "plsh_stream_status", "plsh_last_error"):
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for st in range(6):
+        assert lib.plsh_status_string(st)
+    assert lib.plsh_last_error() is not None
+
+
+@pytest.mark.parametrize("n,H,s,sigma", [(0, 1, 1, [1.0]), (10, 1, 0, [1.0]),
+                                         (10, 1, 65, [1.0]), (10, 1, 2, [0.0]),
+                                         (10, 1, 2, [float("nan")]),
+                                         (10, 1, 2, [float("inf")]),
+                                         (10, 2, 2, [1.0, -3.0])])
+def test_sample_bins_rejects_bad_arguments(lib, n, H, s, sigma):
+    sig = np.asarray(sigma, dtype=np.float64)
+    out = ctypes.c_void_p()
+    st = lib.plsh_sample_bins(n, sig.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+                              H, s, 0, None, ctypes.byref(out))
+    assert st == plsh.PLSH_ERR_INVALID
+    assert out.value is None
+    assert lib.plsh_last_error()
+
+
+def test_bins_from_host_rejects_bad_lists(lib):
+    def call(n, H, s, offsets, starts):
+        off = np.asarray(offsets, dtype=np.int64)
+        stt = np.asarray(starts, dtype=np.int32)
+        out = ctypes.c_void_p()
+        return lib.plsh_bins_from_host(
+            n, H, s, off.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+            stt.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), None, ctypes.byref(out))
+    assert call(8, 1, 1, [0, 3], [1, 4, 8]) == plsh.PLSH_ERR_INVALID   # first != 0
+    assert call(8, 1, 1, [0, 3], [0, 4, 7]) == plsh.PLSH_ERR_INVALID   # last != n
+    assert call(8, 1, 1, [0, 4], [0, 4, 4, 8]) == plsh.PLSH_ERR_INVALID  # not increasing
+    assert call(8, 1, 1, [0, 1], [0]) == plsh.PLSH_ERR_INVALID          # too short
+
+
+def test_attention_rejects_null_and_misaligned(lib):
+    T = plsh._Tensor
+    good = T(256, plsh.PLSH_BF16, 1, 1, 128, 128)
+    bad_align = T(258, plsh.PLSH_BF16, 1, 1, 128, 128)
+    bad_d = T(256, plsh.PLSH_BF16, 1, 1, 128, 96)
+    sig = np.ones(1)
+    sp = sig.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+    for q, o in ((bad_align, good), (bad_d, bad_d)):
+        st = lib.plsh_alibi_exact(ctypes.byref(q), ctypes.byref(good), ctypes.byref(good),
+                                  sp, 1, ctypes.byref(o), None)
+        assert st == plsh.PLSH_ERR_INVALID
+    st = lib.plsh_alibi_attn(ctypes.byref(good), ctypes.byref(good), ctypes.byref(good),
+                             None, 1, ctypes.byref(good), None)
+    assert st == plsh.PLSH_ERR_INVALID
+    # GQA ratio must divide
+    q3 = T(256, plsh.PLSH_BF16, 1, 3, 128, 128)
+    k2 = T(256, plsh.PLSH_BF16, 1, 2, 128, 128)
+    st = lib.plsh_alibi_exact(ctypes.byref(q3), ctypes.byref(k2), ctypes.byref(k2), sp, 1,
+                              ctypes.byref(q3), None)
+    assert st == plsh.PLSH_ERR_INVALID

@@ -1,0 +1,215 @@
+"""CUDA path vs the fp64 oracle, through the C ABI.
+
+Tolerances (elementwise |gpu - oracle| <= atol + rtol |oracle|):
+  bf16 inputs: atol 2e-3, rtol 1e-2   (P and O are rounded to bf16)
+  fp32 inputs: atol 1e-5, rtol 1e-5
+Bin boundaries and draws: bit-exact.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import positional_lsh_approximation_gb300 as plsh
+from positional_lsh_approximation_gb300.inputs import (WORKLOADS, Workload,
+                                                       alibi_sigmas, make_qkv,
+                                                       sample_rows)
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"bf16": (2e-3, 1e-2), "f32": (1e-5, 1e-5)}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    plsh.build()
+    plsh.load()
+
+
+def to_dev(x: np.ndarray, dtype: str) -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(x))
+    t = t.to(torch.bfloat16) if dtype == "bf16" else t
+    return t.cuda()
+
+
+def gather_rows(O: torch.Tensor, rows):
+    rb, rh, ri = (torch.from_numpy(np.asarray(r, dtype=np.int64)).cuda() for r in rows)
+    return O[rb, rh, ri].float().cpu().numpy().astype(np.float64)
+
+
+def assert_close(got, ref, dtype, what=""):
+    atol, rtol = TOL[dtype]
+    err = np.abs(got - ref)
+    bad = err > atol + rtol * np.abs(ref)
+    assert not np.isnan(got).any(), f"{what}: NaN in GPU output"
+    if bad.any():
+        idx = np.argwhere(bad)[:5]
+        raise AssertionError(f"{what}: {bad.sum()} of {bad.size} elements out of "
+                             f"tolerance; max err {err.max():.3e}; first {idx.tolist()}")
+
+
+def run_approx(w: Workload, Q, K, V, bins, path=None, monkeypatch=None):
+    if path is not None:
+        monkeypatch.setenv("PLSH_PATH", path)
+    O = plsh.alibi_attn(to_dev(Q, w.dtype), to_dev(K, w.dtype), to_dev(V, w.dtype),
+                        bins, w.causal)
+    plsh.stream_status()
+    return O
+
+
+# ------------------------------------------------------------------ sampler
+@pytest.mark.parametrize("n,H,s,sig,seed", [
+    (1, 1, 3, [2.0], 0), (31, 2, 5, [0.6, 3.0], 1), (1000, 1, 8, [16.0], 0),
+    (8192, 32, 10, None, 0), (16384, 32, 40, None, 0), (131072, 40, 16, [256.0], 0),
+    (4097, 3, 64, [1e6, 0.9, 50.0], 2**63 + 5)])
+def test_sampler_bit_exact(n, H, s, sig, seed):
+    sigma = alibi_sigmas(H) if sig is None else np.asarray(sig, dtype=np.float64)
+    bins = plsh.sample_bins(n, sigma, s, seed)
+    off, st = bins.to_host()
+    w, u = bins.draws()
+    roff, rst, rw, ru = oracle.sample_bins(n, sigma, s, seed, return_draws=True)
+    assert np.array_equal(w.view(np.uint64), rw.view(np.uint64))
+    assert np.array_equal(u.view(np.uint64), ru.view(np.uint64))
+    assert np.array_equal(off, roff)
+    assert np.array_equal(st, rst)
+    # resampling in place gives a new, equally exact draw
+    bins.resample(sigma * 1.5, seed + 1)
+    off2, st2 = bins.to_host()
+    roff2, rst2 = oracle.sample_bins(n, sigma * 1.5, s, seed + 1)
+    assert np.array_equal(off2, roff2) and np.array_equal(st2, rst2)
+    bins.free()
+
+
+def test_bins_from_host_round_trip():
+    n, H, s = 777, 3, 6
+    off, st = oracle.sample_bins(n, [2.0, 9.0, 70.0], s, seed=4)
+    bins = plsh.bins_from_host(n, H, s, off, st)
+    off2, st2 = bins.to_host()
+    assert np.array_equal(off, off2) and np.array_equal(st, st2)
+
+
+# --------------------------------------------------------- small, all rows
+SMALL = [
+    # name, B, Hq, Hkv, n, d, dtype, causal, s, sigma
+    ("f32_tiny_like", 1, 1, 1, 300, 64, "f32", False, 8, (16.0,)),
+    ("f32_causal_gqa", 2, 4, 2, 260, 128, "f32", True, 5, (0.7, 3.0, 20.0, 90.0)),
+    ("bf16_causal_ragged", 1, 4, 2, 1000, 128, "bf16", True, 10, (1.2, 6.0, 40.0, 300.0)),
+    ("bf16_noncausal_ragged", 2, 2, 1, 777, 128, "bf16", False, 6, (3.0, 150.0)),
+    ("bf16_d64", 1, 2, 1, 513, 64, "bf16", True, 4, (5.0, 60.0)),
+    ("bf16_s64", 1, 2, 2, 640, 128, "bf16", True, 64, (2.0, 30.0)),
+    ("bf16_short", 1, 3, 1, 70, 128, "bf16", True, 3, (1.0, 8.0, 1e5)),
+    ("bf16_one_token", 1, 2, 1, 1, 128, "bf16", True, 2, (4.0, 4.0)),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[c[0] for c in SMALL])
+@pytest.mark.parametrize("path", ["auto", "simt"])
+def test_small_cases_all_rows(case, path, monkeypatch):
+    name, B, Hq, Hkv, n, d, dtype, causal, s, sig = case
+    w = Workload(name, B, Hq, Hkv, n, d, dtype, causal, s, sig, qkv_seed=n + s)
+    Q, K, V = make_qkv(w)
+    sigma = w.sigmas()
+    bins = plsh.sample_bins(n, sigma, s, seed=3)
+    off, st = oracle.sample_bins(n, sigma, s, seed=3)
+    O = run_approx(w, Q, K, V, bins, None if path == "auto" else path, monkeypatch)
+    rows = oracle.all_rows(B, Hq, n)
+    ref = oracle.plsh_attn_rows(Q, K, V, off, st, s, causal, rows)
+    assert_close(gather_rows(O, rows), ref, dtype, f"{name}/{path}")
+
+
+@pytest.mark.parametrize("case", SMALL[:5], ids=[c[0] for c in SMALL[:5]])
+@pytest.mark.parametrize("path", ["auto", "simt"])
+def test_exact_small_all_rows(case, path, monkeypatch):
+    name, B, Hq, Hkv, n, d, dtype, causal, s, sig = case
+    w = Workload(name, B, Hq, Hkv, n, d, dtype, causal, s, sig, qkv_seed=n + 1)
+    Q, K, V = make_qkv(w)
+    sigma = w.sigmas()
+    if path == "simt":
+        monkeypatch.setenv("PLSH_PATH", "simt")
+    O = plsh.alibi_exact(to_dev(Q, dtype), to_dev(K, dtype), to_dev(V, dtype), sigma, causal)
+    plsh.stream_status()
+    rows = oracle.all_rows(B, Hq, n)
+    ref = oracle.alibi_exact_rows(Q, K, V, sigma, causal, rows)
+    assert_close(gather_rows(O, rows), ref, dtype, f"exact {name}/{path}")
+
+
+def test_special_cases_single_bin_and_singletons():
+    n, d = 300, 128
+    w = Workload("sp", 1, 2, 1, n, d, "bf16", True, 1, (1.0,), qkv_seed=9)
+    Q, K, V = make_qkv(w)
+    # one bin [0, n) per head: plain causal softmax attention
+    off = np.array([0, 2, 4], dtype=np.int64)
+    st = np.array([0, n, 0, n], dtype=np.int32)
+    bins = plsh.bins_from_host(n, 2, 1, off, st)
+    O = run_approx(w, Q, K, V, bins)
+    rows = oracle.all_rows(1, 2, n)
+    ref = oracle.plsh_attn_rows(Q, K, V, off, st, 1, True, rows)
+    assert_close(gather_rows(O, rows), ref, "bf16", "single bin")
+    # all singletons: every output row is its own value row
+    s = 3
+    off = np.arange(0, 2 * s * (n + 1) + 1, n + 1, dtype=np.int64)
+    st = np.tile(np.arange(n + 1, dtype=np.int32), 2 * s)
+    bins = plsh.bins_from_host(n, 2, s, off, st)
+    O = run_approx(w, Q, K, V, bins)
+    got = O.float().cpu().numpy()
+    np.testing.assert_array_equal(got[0, 0], V[0, 0])
+    np.testing.assert_array_equal(got[0, 1], V[0, 0])
+
+
+def test_repeated_calls_reuse_queue_and_agree():
+    w = WORKLOADS["mistral"].with_(n=2048)
+    Q, K, V = make_qkv(w)
+    bins = plsh.sample_bins(w.n, w.sigmas(), w.s, 0)
+    q, k, v = to_dev(Q, "bf16"), to_dev(K, "bf16"), to_dev(V, "bf16")
+    outs = [plsh.alibi_attn(q, k, v, bins, True) for _ in range(3)]
+    plsh.stream_status()
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+
+
+# ------------------------------------------------- full sizes, sampled rows
+FULL = ["tiny", "mistral", "qwen_s10", "qwen_s20", "sweep_s1", "sweep_s5",
+        "sweep_s10", "sweep_s20", "sweep_s40", "scout"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled_rows(name):
+    w = WORKLOADS[name]
+    Q, K, V = make_qkv(w)
+    sigma = w.sigmas()
+    bins = plsh.sample_bins(w.n, sigma, w.s, w.hash_seed)
+    off, st = oracle.sample_bins(w.n, sigma, w.s, w.hash_seed)
+    O = run_approx(w, Q, K, V, bins)
+    if name == "tiny":
+        rows = oracle.all_rows(w.B, w.Hq, w.n)
+    else:
+        rows, (h_lo, h_hi) = sample_rows(w, per_head=24 if name == "scout" else 48)
+        # every row of batch 0 for the smallest-sigma head, and for the
+        # largest-sigma head where the oracle stays within seconds
+        full_heads = [h_lo] + ([h_hi] if w.n * w.s <= 200_000 else [])
+        rb = [rows[0]] + [np.zeros(w.n, np.int32) for _ in full_heads]
+        rh = [rows[1]] + [np.full(w.n, h, np.int32) for h in full_heads]
+        ri = [rows[2]] + [np.arange(w.n, dtype=np.int32) for _ in full_heads]
+        rows = (np.concatenate(rb), np.concatenate(rh), np.concatenate(ri))
+    ref = oracle.plsh_attn_rows(Q, K, V, off, st, w.s, w.causal, rows)
+    assert_close(gather_rows(O, rows), ref, w.dtype, name)
+
+
+@pytest.mark.parametrize("name", ["tiny", "mistral", "qwen_s10", "sweep_s10", "scout"])
+def test_exact_full_size_sampled_rows(name):
+    w = WORKLOADS[name]
+    Q, K, V = make_qkv(w)
+    sigma = w.sigmas()
+    O = plsh.alibi_exact(to_dev(Q, w.dtype), to_dev(K, w.dtype), to_dev(V, w.dtype),
+                         sigma, w.causal)
+    plsh.stream_status()
+    if name == "tiny":
+        rows = oracle.all_rows(w.B, w.Hq, w.n)
+    else:
+        rows, _ = sample_rows(w, per_head=4 if name == "scout" else 12)
+    ref = oracle.alibi_exact_rows(Q, K, V, sigma, w.causal, rows)
+    assert_close(gather_rows(O, rows), ref, w.dtype, "exact " + name)
