@@ -1,0 +1,435 @@
+"""Benchmark of the Positional LSH approximate-ALiBi hot path on one GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+redraw the s hashes per head and rebuild their bin records
+(plsh_bins_resample: draw, bitmap, neighbour scans), then the fused block
+attention with its in-kernel work queue and O / l epilogue (plsh_alibi_attn).
+Inputs are resident in HBM when the timed region starts; L2 is flushed
+(256 MiB write) between timed steps, outside the per-step events.
+
+Prints ONE JSON line (rank 0).  --impl reference times the fp64 CPU oracle
+on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from positional_lsh_approximation_gb300.inputs import WORKLOADS, make_qkv  # noqa: E402
+
+METRIC = "approx-ALiBi attn tokens/s (n=8k, 32h, d=128, s=10) & % of bf16 TC roofline, 1 GB300"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------- helpers
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {
+            "hbm_gbs": float(d.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])),
+            "bf16_tflops": float(d.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])),
+            "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained",
+                                                 FALLBACK_PEAKS["bf16_tflops_sustained"])),
+            "source": "measured",
+        }
+    return dict(FALLBACK_PEAKS, source="fallback")
+
+
+def work_counts(w, offsets, starts):
+    """Algorithmic work of one launch from the actual bins.
+
+    F_block = 4 d B sum_h sum_t sum_bins pairs(b), pairs(b) = b(b+1)/2 when
+    causal else b^2 (QK^T and PV per (i, j) pair in a block); bytes = Q, K, V
+    read once and O written once.  Also the tensor-core work the kernel
+    executes: per (b, h, 128-row tile) every key tile of the union envelope,
+    three 128x128x128 products (S, P_hi V, P_lo V)."""
+    lens = np.diff(starts.astype(np.int64))
+    # drop the terminal-to-next-hash differences: use per-hash slices
+    pairs = 0
+    H, s = w.Hq, w.s
+    env_tiles = 0
+    QT = (w.n + 127) // 128
+    for h in range(H):
+        lo_min = np.full(QT, np.iinfo(np.int64).max)
+        for t in range(s):
+            st = starts[offsets[h * s + t]:offsets[h * s + t + 1]].astype(np.int64)
+            b = np.diff(st)
+            pairs += int((b * (b + 1) // 2).sum() if w.causal else (b * b).sum())
+            i0 = np.arange(QT) * 128
+            lo = st[np.searchsorted(st, i0, side="right") - 1]
+            lo_min = np.minimum(lo_min, lo)
+        if w.causal:
+            env_tiles += int((np.arange(QT) - lo_min // 128 + 1).sum())
+        else:
+            env_tiles += int(QT * QT)  # upper bound, not used for the headline
+    f_block = 4.0 * w.d * w.B * pairs
+    e = 2 if w.dtype == "bf16" else 4
+    bytes_ = w.B * w.n * w.d * e * (2 * w.Hq + 2 * w.Hkv)
+    mma = w.B * env_tiles * 3 * 2.0 * 128 * 128 * 128
+    return f_block, bytes_, mma, env_tiles * w.B
+
+
+class ClockSampler:
+    """nvidia-smi samples during the timed region (clocks and throttle reasons)."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def kernel_traffic():
+    """dram bytes per launch of the fused kernel from the committed ncu summary,
+    valid only for the exact kernel source it was taken from."""
+    path = os.path.join(ROOT, "profiles", "attn_tc_traffic.json")
+    src = os.path.join(ROOT, "positional_lsh_approximation_gb300", "csrc", "attn_tc.cu")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    with open(src, "rb") as f:
+        digest = hashlib.sha256(f.read()).hexdigest()[:16]
+    if d.get("source_sha256_16") != digest:
+        return None
+    return d.get("traffic_bytes_per_launch")
+
+
+# ------------------------------------------------------------- our arm
+def run_ours(args, rank, world):
+    import torch
+    import torch.distributed as dist
+
+    import positional_lsh_approximation_gb300 as plsh
+
+    w = WORKLOADS[args.workload]
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    plsh.build()
+    Qn, Kn, Vn = make_qkv(w)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    Q = torch.from_numpy(Qn).to(tdt).to(dev)
+    K = torch.from_numpy(Kn).to(tdt).to(dev)
+    V = torch.from_numpy(Vn).to(tdt).to(dev)
+    O = torch.empty_like(Q)
+    sigma = w.sigmas()
+    stream = torch.cuda.current_stream()
+    bins = plsh.sample_bins(w.n, sigma, w.s, w.hash_seed)
+    offsets, starts = bins.to_host()
+    f_block, bytes_, mma_exec, tiles = work_counts(w, offsets, starts)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    seed = w.hash_seed   # the same draw every step, so F_block is exact for each
+
+    for i in range(args.warmup):
+        bins.resample(sigma, seed)
+        plsh.alibi_attn(Q, K, V, bins, w.causal, out=O)
+    plsh.stream_status()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(dev.index) as clocks:
+        for i in range(args.steps):
+            flush.zero_()
+            e0, e1, e2 = ev[i]
+            e0.record(stream)
+            bins.resample(sigma, seed)
+            e1.record(stream)
+            plsh.alibi_attn(Q, K, V, bins, w.causal, out=O)
+            e2.record(stream)
+        torch.cuda.synchronize()
+    plsh.stream_status()
+    step_ms = [a.elapsed_time(c) for a, b, c in ev]
+    attn_ms = [b.elapsed_time(c) for a, b, c in ev]
+    sample_ms = [a.elapsed_time(b) for a, b, c in ev]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    tokens = w.B * w.n * world
+    value = tokens * args.steps / (total_ms / 1e3)
+    attn_avg_s = statistics.mean(attn_ms) / 1e3
+
+    # end to end through the public API with host buffers (pinned)
+    Qh, Kh, Vh = (x.cpu().pin_memory() for x in (Q, K, V))
+    Oh = torch.empty(Q.shape, dtype=Q.dtype).pin_memory()
+    for i in range(2):
+        bins.resample(sigma, seed)
+        plsh.alibi_attn(Qh, Kh, Vh, bins, w.causal, out=Oh)
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for i in range(args.steps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        bins.resample(sigma, seed)
+        plsh.alibi_attn(Qh, Kh, Vh, bins, w.causal, out=Oh)
+        b.record(stream)
+        b.synchronize()
+        e2e_ms.append(a.elapsed_time(b))
+    h2d = sum(x.numel() * x.element_size() for x in (Q, K, V))
+    d2h = O.numel() * O.element_size()
+
+    # exact dense ALiBi on the same inputs, and the approximation error
+    E = torch.empty_like(Q)
+    plsh.alibi_exact(Q, K, V, sigma, w.causal, out=E)
+    torch.cuda.synchronize()
+    ex_ms = []
+    for i in range(max(3, min(args.steps, 10))):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        plsh.alibi_exact(Q, K, V, sigma, w.causal, out=E)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ex_ms.append(a.elapsed_time(b))
+    plsh.stream_status()
+    bins.resample(sigma, w.hash_seed)
+    plsh.alibi_attn(Q, K, V, bins, w.causal, out=O)
+    torch.cuda.synchronize()
+    diff = (O.float() - E.float())
+    approx_err = {
+        "max_abs": float(diff.abs().max()),
+        "mean_abs": float(diff.abs().mean()),
+        "rel_fro": float(diff.norm() / E.float().norm()),
+    }
+    ex_avg_s = statistics.mean(ex_ms) / 1e3
+    ex_flops = 4.0 * w.d * w.B * w.Hq * (w.n * (w.n + 1) / 2 if w.causal else w.n * w.n)
+
+    pk = peaks()
+    peak_tf = pk["bf16_tflops"]
+    achieved_tf = f_block / attn_avg_s / 1e12
+    result = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded N(0,1) Q/K/V of the workload's shape, no weights)",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "n": w.n,
+                   "d": w.d, "s": w.s, "causal": w.causal,
+                   "sigma": "ALiBi slopes sigma_h = 2^(8h/H)" if not w.sigma else list(w.sigma),
+                   "hashes": "redrawn on the device every step (same seed)",
+                   "l2": "flushed between timed steps (256 MiB write)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {
+            "bound": "tensor",
+            "achieved": achieved_tf,
+            "peak": peak_tf,
+            "unit": "TFLOP/s",
+            "frac": achieved_tf / peak_tf,
+            "traffic": kernel_traffic(),
+            "kernel": "attn_tc_kernel<false,true>",
+            "flops_per_launch": f_block,
+            "kernel_ms": attn_avg_s * 1e3,
+            "peak_source": pk["source"] + " (burst, kernel timed alone)",
+            "hbm_frac": bytes_ / attn_avg_s / 1e9 / pk["hbm_gbs"],
+            "bytes_per_launch": bytes_,
+            "mma_flops_executed": mma_exec,
+            "mma_frac_executed": mma_exec / attn_avg_s / 1e12 / peak_tf,
+            "tiles_executed": tiles,
+        },
+        "sample_ms": statistics.mean(sample_ms),
+        "e2e": {"value": w.B * w.n * world / (statistics.mean(e2e_ms) / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": statistics.mean(e2e_ms)},
+        "gpu_launches": 4 * args.steps,
+        "exact": {"tokens_per_s": w.B * w.n / ex_avg_s, "ms": ex_avg_s * 1e3,
+                  "tflops": ex_flops / ex_avg_s / 1e12,
+                  "frac": ex_flops / ex_avg_s / 1e12 / peak_tf},
+        "approx_error_vs_exact": approx_err,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and not args.no_cpu:
+        result["cpu_baseline"] = cpu_baseline(w, Qn, Kn, Vn, offsets, starts, args.cpu_seconds)
+    return result
+
+
+# ---------------------------------------------------------- oracle on CPU
+def cpu_baseline(w, Qn, Kn, Vn, offsets, starts, budget_s):
+    """The fp64 oracle as it stands, on every host core, over a bounded sample
+    of token positions (all heads of batch element 0)."""
+    import oracle
+    oracle.build()
+    cores = os.cpu_count() or 1
+    oracle.set_threads(cores)
+    rng = np.random.default_rng(0)
+    npos = 16
+    elapsed = 0.0
+    done = 0
+    while True:
+        pos = rng.integers(0, w.n, size=npos).astype(np.int32)
+        rb = np.zeros(npos * w.Hq, np.int32)
+        rh = np.repeat(np.arange(w.Hq, dtype=np.int32), npos)
+        ri = np.tile(pos, w.Hq)
+        t0 = time.perf_counter()
+        oracle.plsh_attn_rows(Qn, Kn, Vn, offsets, starts, w.s, w.causal, (rb, rh, ri))
+        dt = time.perf_counter() - t0
+        elapsed += dt
+        done += npos
+        if elapsed >= budget_s or done >= w.B * w.n:
+            break
+        npos = int(min(4096, max(npos * 2, npos * (budget_s - elapsed) / max(dt, 1e-3) * 0.5)))
+    return {"value": done / elapsed, "unit": "tokens/s", "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": f"{done} random token positions x all {w.Hq} heads of batch 0, "
+                      f"fp64, {elapsed:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    w = WORKLOADS[args.workload]
+    import oracle
+    Qn, Kn, Vn = make_qkv(w)
+    offsets, starts = oracle.sample_bins(w.n, w.sigmas(), w.s, w.hash_seed)
+    oracle.build()
+    oracle.set_threads(os.cpu_count() or 1)
+    rng = np.random.default_rng(1)
+    per_step = args.ref_positions
+    for i in range(args.warmup):
+        pos = rng.integers(0, w.n, size=max(1, per_step // 4)).astype(np.int32)
+        oracle.plsh_attn_rows(Qn, Kn, Vn, offsets, starts, w.s, w.causal,
+                              (np.zeros(pos.size * w.Hq, np.int32),
+                               np.repeat(np.arange(w.Hq, dtype=np.int32), pos.size),
+                               np.tile(pos, w.Hq)))
+    times = []
+    for i in range(args.steps):
+        pos = rng.integers(0, w.n, size=per_step).astype(np.int32)
+        rows = (np.zeros(per_step * w.Hq, np.int32),
+                np.repeat(np.arange(w.Hq, dtype=np.int32), per_step), np.tile(pos, w.Hq))
+        t0 = time.perf_counter()
+        oracle.plsh_attn_rows(Qn, Kn, Vn, offsets, starts, w.s, w.causal, rows)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = per_step * args.steps / total
+    sample = (f"{per_step} random token positions x all {w.Hq} heads per step "
+              f"(of {w.B * w.n} tokens), fp64 oracle")
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": total / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) Q/K/V of the workload's shape, no weights)",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "n": w.n,
+                   "d": w.d, "s": w.s, "causal": w.causal},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "kind": "oracle",
+                         "cores": oracle.max_threads(), "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="mistral", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-positions", type=int, default=96)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    res = run_ours(args, rank, world)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

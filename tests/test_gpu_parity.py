@@ -100,7 +100,9 @@ SMALL = [
     ("bf16_causal_ragged", 1, 4, 2, 1000, 128, "bf16", True, 10, (1.2, 6.0, 40.0, 300.0)),
     ("bf16_noncausal_ragged", 2, 2, 1, 777, 128, "bf16", False, 6, (3.0, 150.0)),
     ("bf16_d64", 1, 2, 1, 513, 64, "bf16", True, 4, (5.0, 60.0)),
+    ("bf16_s48", 1, 2, 2, 640, 128, "bf16", True, 48, (2.0, 30.0)),
     ("bf16_s64", 1, 2, 2, 640, 128, "bf16", True, 64, (2.0, 30.0)),
+    ("bf16_noncausal_s30", 1, 2, 1, 400, 128, "bf16", False, 30, (0.8, 40.0)),
     ("bf16_short", 1, 3, 1, 70, 128, "bf16", True, 3, (1.0, 8.0, 1e5)),
     ("bf16_one_token", 1, 2, 1, 1, 128, "bf16", True, 2, (4.0, 4.0)),
 ]
