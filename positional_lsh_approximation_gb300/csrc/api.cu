@@ -221,6 +221,96 @@ plsh_status check_qkvo(const plsh_tensor* Q, const plsh_tensor* K, const plsh_te
   return PLSH_OK;
 }
 
+// Items of the tensor-core kernel: two 128-row query tiles sharing one KV
+// head.  Heads of a KV group pair up (sorted by sigma so that paired heads
+// have similar key envelopes); an odd group's last head pairs its own row
+// tiles.  Ordered by expected cost, largest first, so that the dynamic queue
+// balances like longest-processing-time scheduling.
+std::vector<int4> build_items(int B, int Hq, int Hkv, int QT, bool exact,
+                              const std::vector<double>& sigma) {
+  const int G = Hq / Hkv;
+  std::vector<int4> items;
+  std::vector<double> cost;
+  items.reserve((size_t)B * Hq * QT / 2 + B * Hkv);
+  for (int b = 0; b < B; ++b) {
+    for (int kvh = 0; kvh < Hkv; ++kvh) {
+      std::vector<int> heads(G);
+      std::iota(heads.begin(), heads.end(), kvh * G);
+      if (!exact)
+        std::stable_sort(heads.begin(), heads.end(),
+                         [&](int x, int y) { return sigma[x] > sigma[y]; });
+      for (int pr = 0; pr + 1 < G; pr += 2) {
+        const int hA = heads[pr], hB = heads[pr + 1];
+        for (int qt = 0; qt < QT; ++qt) {
+          items.push_back(make_int4(b, hA | (hB << 16), qt, qt));
+          cost.push_back(exact ? (double)qt : std::max(sigma[hA], sigma[hB]) * 1e6 + qt);
+        }
+      }
+      if (G % 2) {
+        const int hL = heads[G - 1];
+        for (int qt = 0; qt < QT; qt += 2) {
+          const int qtB = qt + 1 < QT ? qt + 1 : -1;
+          items.push_back(make_int4(b, hL | (hL << 16), qt, qtB));
+          cost.push_back(exact ? (double)std::max(qt, qtB) : sigma[hL] * 1e6 + qt);
+        }
+      }
+    }
+  }
+  std::vector<size_t> order(items.size());
+  std::iota(order.begin(), order.end(), 0);
+  std::stable_sort(order.begin(), order.end(),
+                   [&](size_t x, size_t y) { return cost[x] > cost[y]; });
+  std::vector<int4> sorted(items.size());
+  for (size_t k = 0; k < order.size(); ++k) sorted[k] = items[order[k]];
+  return sorted;
+}
+
+// Device copy of the item table for this shape and head order (built and
+// uploaded on first use, then reused).
+plsh_status item_table(plsh::DeviceCtx* ctx, int B, int Hq, int Hkv, int QT, bool exact,
+                       const std::vector<double>& sigma, cudaStream_t st,
+                       const int4** out, int* count) {
+  // the table depends on the shape and, for the approximate kernel, on the
+  // order of sigma inside each KV group and across heads
+  std::string key = std::to_string(exact) + ":" + std::to_string(B) + ":" + std::to_string(Hq) +
+                    ":" + std::to_string(Hkv) + ":" + std::to_string(QT);
+  if (!exact) {
+    std::vector<int> rank(Hq);
+    std::iota(rank.begin(), rank.end(), 0);
+    std::stable_sort(rank.begin(), rank.end(),
+                     [&](int x, int y) { return sigma[x] > sigma[y]; });
+    key.push_back(':');
+    for (int h : rank) key += std::to_string(h) + ",";
+  }
+  std::lock_guard<std::mutex> lk(g_ctx_mu);
+  auto it = ctx->tables.find(key);
+  if (it == ctx->tables.end()) {
+    if (ctx->tables.size() >= plsh::kMaxTables) {
+      auto victim = ctx->tables.begin();
+      for (auto jt = ctx->tables.begin(); jt != ctx->tables.end(); ++jt)
+        if (jt->second.last_use < victim->second.last_use) victim = jt;
+      cudaDeviceSynchronize();
+      cudaFree(victim->second.dev);
+      ctx->tables.erase(victim);
+    }
+    plsh::ItemTable t;
+    t.host = build_items(B, Hq, Hkv, QT, exact, sigma);
+    plsh_status s = dev_alloc((void**)&t.dev, sizeof(int4) * t.host.size(), "item table");
+    if (s != PLSH_OK) return s;
+    cudaError_t e = cudaMemcpyAsync(t.dev, t.host.data(), sizeof(int4) * t.host.size(),
+                                    cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) {
+      cudaFree(t.dev);
+      return cuda_fail(e, "item table upload");
+    }
+    it = ctx->tables.emplace(key, std::move(t)).first;
+  }
+  it->second.last_use = ++ctx->table_clock;
+  *out = it->second.dev;
+  *count = (int)it->second.host.size();
+  return PLSH_OK;
+}
+
 enum class Path { Auto, Simt, Tc };
 
 Path path_override() {
@@ -254,7 +344,6 @@ plsh_status run_attention(const plsh_tensor* Q, const plsh_tensor* K, const plsh
     a.rec = bins->d_rec;
     a.s = bins->s;
     a.W = bins->W;
-    a.head_order = bins->d_head_order;
   }
   a.err = ctx->d_err;
   a.wait_ns = ctx->wait_ns;
@@ -269,6 +358,13 @@ plsh_status run_attention(const plsh_tensor* Q, const plsh_tensor* K, const plsh
   if (path == Path::Tc && !tc_ok)
     return fail(PLSH_ERR_UNSUPPORTED, "tensor-core path needs bf16, d = 128 and s within "
                                       "its shared-memory budget");
+  if (path == Path::Tc) {
+    const int QT = (int)((Q->n + 127) / 128);
+    plsh_status s1 = item_table(ctx, a.B, a.Hq, a.Hkv, QT, a.exact != 0,
+                                bins ? bins->sigma_host : std::vector<double>(), st,
+                                &a.items, &a.num_items);
+    if (s1 != PLSH_OK) return s1;
+  }
   cudaError_t e = path == Path::Tc ? plsh::launch_attn_tc(a, slopes, ctx->num_sms, st)
                                    : plsh::launch_attn_simt(a, slopes, Q->dtype, st);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");

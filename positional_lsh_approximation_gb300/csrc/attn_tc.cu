@@ -21,26 +21,31 @@
 // Exact ALiBi (the dense comparator) runs on the same pipeline with weight
 // e^{S_ij - |i-j|/sigma_h} over every key tile.
 //
-// Pipeline (one persistent CTA per SM, 6 warps):
-//   warp 4      producer: pops work items (b, h, 128-row query tile) from a
-//               global queue ordered by expected cost, stages the item's bin
-//               records in shared memory, finds its key envelope, TMA-loads Q
-//               (two item stages) and K/V tiles (two stages each) from the
-//               diagonal tile down;
-//   warp 5      one thread issues tcgen05.mma: S = Q K^T into one of two TMEM
-//               score buffers, then O += P V into the TMEM accumulator
-//               (tcgen05 MMAs of one thread execute in issue order, so the
-//               next S into a buffer lands after the P V that reads it);
-//   warps 0-3   one thread per query row: tcgen05.ld of the score row, running
-//               max over the valid keys, lazy rescale of O in TMEM (only when
-//               the max grows by more than 2^8), P = 2^(x - m) split into two
-//               bf16 terms P = P_hi + P_lo written back over the consumed
-//               score columns, row sums in fp32, and the final O / l epilogue.
+// One persistent CTA per SM, 10 warps, two 128-row query tiles A and B per
+// work item (two heads of one KV group at the same rows, or two row tiles of
+// one head), sharing every K/V tile:
+//   warp 8      producer: pops items from a global queue in cost order,
+//               stages the rows' bin records in shared memory, finds the key
+//               envelope, TMA-loads Q_A, Q_B and the K/V tiles (a ring of
+//               three 32 KB slots) from the diagonal tile down;
+//   warp 9      one thread issues tcgen05.mma in the order
+//               S_A(g) S_B(g) PV_A(g) S_A(g+1) PV_B(g) S_B(g+1) ...
+//               so that while one warpgroup turns its scores into weights the
+//               tensor core works for the other (tcgen05 MMAs of one thread
+//               execute in issue order: the commit that follows S_X(g) also
+//               proves PV_X(g-1) has landed);
+//   warps 0-3   softmax of tile A, warps 4-7 softmax of tile B: one thread
+//               per row, tcgen05.ld of the score row, running max over the
+//               valid keys, lazy rescale of O in TMEM (only when the max grows
+//               by more than 2^8), P = c 2^(x - m) split into two bf16 terms
+//               P_hi + P_lo written back over the consumed score columns,
+//               fp32 row sums, and the O / l epilogue.
 //   O += P_hi V + P_lo V runs as two tensor-core products with A read from
 //   TMEM: a single bf16 P carries a 2^-9 relative error per weight, which
 //   shows in rows whose few keys cancel; the pair carries about 2^-17.
-// Every wait on an mbarrier is bounded; on expiry the CTA raises the library
-// error flag, drains its in-flight copies and MMAs, frees TMEM and exits.
+// TMEM columns: S_A | S_B | O_A | O_B.  Every wait on an mbarrier is bounded;
+// on expiry the CTA raises the library error flag, drains its in-flight copies
+// and MMAs, frees TMEM and exits.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <limits.h>
@@ -60,32 +65,39 @@ using namespace ptx;
 constexpr int BM = 128;      // query rows per tile (MMA M)
 constexpr int BN = 128;      // keys per tile (MMA N of QK^T, K of PV)
 constexpr int HD = 128;      // head dim (MMA K of QK^T, N of PV)
-constexpr int kThreads = 192;
+constexpr int kWarps = 11;
+constexpr int kThreads = kWarps * 32;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kSchedWarp = 10;
+constexpr int kRing = 3;                         // work items in flight
+constexpr int kSlots = 3;                        // K/V tile ring
 constexpr uint32_t kTileBytes = BM * HD * 2;     // 32 KB bf16 tile
 constexpr uint32_t kHalfBytes = kTileBytes / 2;  // one 64-column TMA box
-constexpr uint32_t OFF_Q = 0;                        // two item stages
-constexpr uint32_t OFF_K = OFF_Q + 2 * kTileBytes;   // two tile stages
-constexpr uint32_t OFF_V = OFF_K + 2 * kTileBytes;   // two tile stages
-constexpr uint32_t OFF_BP = OFF_V + 2 * kTileBytes;
-constexpr uint32_t kTmemCols = 512;   // S0 | S1 | O | unused; P over S
+constexpr uint32_t OFF_Q = 0;                          // Q_A, Q_B
+constexpr uint32_t OFF_KV = OFF_Q + 2 * kTileBytes;    // ring of kSlots
+constexpr uint32_t OFF_BP = OFF_KV + kSlots * kTileBytes;
+constexpr uint32_t kTmemCols = 512;   // S_A | S_B | O_A | O_B; P over S
 constexpr uint32_t kColO = 256;
 constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (factor 256)
 constexpr unsigned FULL = 0xffffffffu;
 constexpr int kWordsPerTile = BM / 32;
 
 enum {
-  B_QFULL = 0, B_QFULL1, B_QEMPTY, B_QEMPTY1, B_KFULL, B_KFULL1, B_KEMPTY,
-  B_KEMPTY1, B_VFULL, B_VFULL1, B_VEMPTY, B_VEMPTY1, B_SFULL, B_SFULL1,
-  B_PFULL, B_PVDONE, B_IFULL, B_IFULL1, B_IEMPTY, B_IEMPTY1, B_DRAIN, NUM_BARS
+  B_QFULL = 0, B_QFULL1, B_QEMPTY, B_QEMPTY1, B_KVFULL, B_KVFULL_END = B_KVFULL + kSlots,
+  B_KVEMPTY = B_KVFULL_END, B_KVEMPTY_END = B_KVEMPTY + kSlots,
+  B_SFULL = B_KVEMPTY_END, B_SFULL1, B_PFULL, B_PFULL1, B_ODONE, B_ODONE1,
+  B_IFULL, B_IFULL_END = B_IFULL + kRing, B_IEMPTY = B_IFULL_END,
+  B_IEMPTY_END = B_IEMPTY + kRing, B_DRAIN = B_IEMPTY_END, NUM_BARS
 };
 
 struct Item {
-  int valid, b, h, qt, kt_lo, kt_hi;
+  int valid, b, hA, hB, qtA, qtB, kt_lo, kt_hi;
 };
 
 struct Ctl {
   uint64_t bars[NUM_BARS];
-  Item ring[2];
+  Item ring[kRing];
   uint32_t tmem_base;
   int abort;
 };
@@ -93,24 +105,24 @@ struct Ctl {
 struct TcParams {
   AttnArgs a;
   float slope_log2[512];   // exact mode: log2(e) / sigma_h
-  int num_items;
   int QT;                  // query tiles per (b, h)
 };
 
-// Sorted bin starts (and ends when not causal) of every row: [lists][s][BM].
-__host__ __device__ constexpr uint32_t bp_bytes(int s, bool exact, bool causal) {
-  return exact ? 0u : (uint32_t)(causal ? 1 : 2) * (uint32_t)s * BM * 4u;
+// Sorted bin starts (and ends when not causal) of every row of both tiles:
+// [tile][lists][s][BM] int32.
+__host__ __device__ constexpr uint32_t bp_bytes(int s, bool exact, bool causal, int sreg) {
+  return (exact || sreg > 0) ? 0u : 2u * (uint32_t)(causal ? 1 : 2) * (uint32_t)s * BM * 4u;
 }
-// Bin records of the item's 128 rows, one ring slot per item: [2][s][4] x 16 B.
+// Bin records of both tiles' rows, per item slot: [kRing][2 tiles][s][4] x 16 B.
 __host__ __device__ constexpr uint32_t stage_bytes(int s, bool exact) {
-  return exact ? 0u : 2u * (uint32_t)s * kWordsPerTile * 16u;
+  return exact ? 0u : 2u * kRing * (uint32_t)s * kWordsPerTile * 16u;
 }
 
 __device__ __forceinline__ Item read_item(const Ctl* ctl, int slot) {
   const volatile int* v = reinterpret_cast<const volatile int*>(&ctl->ring[slot]);
   Item it;
-  it.valid = v[0]; it.b = v[1]; it.h = v[2]; it.qt = v[3];
-  it.kt_lo = v[4]; it.kt_hi = v[5];
+  it.valid = v[0]; it.b = v[1]; it.hA = v[2]; it.hB = v[3];
+  it.qtA = v[4]; it.qtB = v[5]; it.kt_lo = v[6]; it.kt_hi = v[7];
   return it;
 }
 
@@ -123,7 +135,55 @@ __device__ __forceinline__ BinRecord unpack_record(const uint4& rv) {
   return rc;
 }
 
-template <bool EXACT, bool CAUSAL>
+// Bit e set when key jc + e of a row whose keys are [jc + ea, jc + eb] takes
+// part.
+__device__ __forceinline__ uint32_t key_mask(int ea, int eb, bool row_ok) {
+  if (!row_ok || ea > 31 || eb < 0 || ea > eb) return 0u;
+  const uint32_t up = eb >= 31 ? 0xffffffffu : ((2u << eb) - 1u);
+  const uint32_t dn = ea <= 0 ? 0xffffffffu : ~((1u << ea) - 1u);
+  return up & dn;
+}
+
+// Multiplies the chunk's weights by the running step count c(e): base plus
+// the binary planes of step multiplicities at each key (up) minus those of
+// bin ends (dn, non-causal only), L planes in use.
+
+// Adds one step at the positions of `m` to a five-plane binary counter.
+__device__ __forceinline__ void plane_add(uint32_t (&pl)[5], uint32_t m) {
+#pragma unroll
+  for (int b = 0; b < 5; ++b) {
+    const uint32_t c = pl[b] & m;
+    pl[b] ^= m;
+    m = c;
+  }
+}
+template <int L, bool CAUSAL>
+__device__ __forceinline__ void scale_by_count(float (&pv)[32], float base,
+                                               const uint32_t (&up)[5],
+                                               const uint32_t (&dn)[5]) {
+  float cf = base;
+#pragma unroll
+  for (int e2 = 0; e2 < 16; ++e2) {
+    float c2[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t bit = 1u << (2 * e2 + h);
+#pragma unroll
+      for (int b = 0; b < L; ++b) {
+        if (up[b] & bit) cf += (float)(1 << b);
+        if (!CAUSAL && (dn[b] & bit)) cf -= (float)(1 << b);
+      }
+      c2[h] = cf;
+    }
+    const uint64_t p2 = f2_mul(f2_pack(pv[2 * e2], pv[2 * e2 + 1]), f2_pack(c2[0], c2[1]));
+    f2_unpack(p2, pv[2 * e2], pv[2 * e2 + 1]);
+  }
+}
+
+// SREG > 0: each row keeps its s <= SREG bin starts (and ends) in registers,
+// unsorted, and counts them per chunk; SREG == 0: sorted lists in shared
+// memory walked by pointers (any s).
+template <bool EXACT, bool CAUSAL, int SREG>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                const __grid_constant__ CUtensorMap tmK,
@@ -137,8 +197,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
   uint8_t* smem = smem_raw + (sbase - raw_u32);
   const int s = a.s;
   int* bp = reinterpret_cast<int*>(smem + OFF_BP);
-  uint4* stage = reinterpret_cast<uint4*>(smem + OFF_BP + bp_bytes(s, EXACT, CAUSAL));
-  Ctl* ctl = reinterpret_cast<Ctl*>(smem + OFF_BP + bp_bytes(s, EXACT, CAUSAL) +
+  uint4* stage = reinterpret_cast<uint4*>(smem + OFF_BP + bp_bytes(s, EXACT, CAUSAL, SREG));
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + OFF_BP + bp_bytes(s, EXACT, CAUSAL, SREG) +
                                     stage_bytes(s, EXACT));
   auto bar = [&](int k) { return smem_u32(&ctl->bars[k]); };
   volatile int* abort = &ctl->abort;
@@ -148,25 +208,30 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
     for (int k = 0; k < 2; ++k) {
       mbar_init(bar(B_QFULL + k), 1);
       mbar_init(bar(B_QEMPTY + k), 1);
-      mbar_init(bar(B_KFULL + k), 1);
-      mbar_init(bar(B_KEMPTY + k), 1);
-      mbar_init(bar(B_VFULL + k), 1);
-      mbar_init(bar(B_VEMPTY + k), 1);
-      mbar_init(bar(B_SFULL + k), 1);
-      mbar_init(bar(B_IFULL + k), 1);
-      mbar_init(bar(B_IEMPTY + k), 1 + BM);
     }
-    mbar_init(bar(B_PFULL), BM);
-    mbar_init(bar(B_PVDONE), 1);
+    for (int k = 0; k < kSlots; ++k) {
+      mbar_init(bar(B_KVFULL + k), 1);
+      mbar_init(bar(B_KVEMPTY + k), 1);
+    }
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(bar(B_SFULL + k), 1);
+      mbar_init(bar(B_PFULL + k), BM);
+      mbar_init(bar(B_ODONE + k), 1);
+    }
+    for (int k = 0; k < kRing; ++k) {
+      mbar_init(bar(B_IFULL + k), 1);
+      // released by the producer, the MMA thread and every softmax thread
+      mbar_init(bar(B_IEMPTY + k), 2 + 2 * BM);
+    }
     mbar_init(bar(B_DRAIN), 1);
     ctl->abort = 0;
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == kProducerWarp && lane == 0) {
     prefetch_tensormap(&tmQ);
     prefetch_tensormap(&tmK);
     prefetch_tensormap(&tmV);
@@ -175,17 +240,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
-  const int n = a.n, Hq = a.Hq, Hkv = a.Hkv, B = a.B;
-  const int QT = p.QT;
+  const int n = a.n, Hq = a.Hq, Hkv = a.Hkv;
 
-  if (warp == 4) {
-    // ------------------------------------------------------------ producer
-    int g = 0;
-    int q_issued[2] = {0, 0}, k_issued[2] = {0, 0}, v_issued[2] = {0, 0};
+  if (warp == kSchedWarp) {
+    // ----------------------------------------------------------- scheduler
+    // pops items, stages the rows' bin records, finds the key envelope and
+    // publishes the item up to kRing - 1 items ahead of its consumers
     bool ok = true;
     for (int seq = 0;; ++seq) {
-      const int slot = seq & 1;
-      const uint32_t use = (uint32_t)seq >> 1;
+      const int slot = seq % kRing;
+      const uint32_t use = (uint32_t)(seq / kRing);
       int idx = 0;
       if (lane == 0) {
         ok = mbar_wait(bar(B_IEMPTY + slot), (use & 1u) ^ 1u, abort, lim);
@@ -194,183 +258,263 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       ok = __shfl_sync(FULL, (int)ok, 0) != 0;
       idx = __shfl_sync(FULL, idx, 0);
       if (!ok) break;
-      if (idx >= p.num_items) {
+      if (idx >= a.num_items) {
         if (lane == 0) {
           ctl->ring[slot].valid = 0;
           mbar_arrive(bar(B_IFULL + slot));
         }
         break;
       }
-      int b, h, qt;
-      if (EXACT) {
-        // longest rows first: query tiles in descending order
-        qt = QT - 1 - idx / (B * Hq);
-        const int rem = idx % (B * Hq);
-        b = rem / Hq;
-        h = rem % Hq;
-      } else {
-        // heads in descending expected work, then every (b, query tile)
-        const int hh = idx / (B * QT);
-        const int rem = idx % (B * QT);
-        h = a.head_order[hh];
-        b = rem / QT;
-        qt = rem % QT;
-      }
-      const int i0 = qt * BM;
+      const int4 e4 = __ldg(a.items + idx);
+      const int b = e4.x, hA = e4.y & 0xffff, hB = (e4.y >> 16) & 0xffff;
+      const int qtA = e4.z, qtB = e4.w;          // qtB < 0: tile B unused
+      const int qmax = max(qtA, qtB);
       int kt_lo, kt_hi;
       if (EXACT) {
         kt_lo = 0;
-        kt_hi = CAUSAL ? qt + 1 : (n + BN - 1) / BN;
+        kt_hi = CAUSAL ? qmax + 1 : (n + BN - 1) / BN;
       } else {
-        // stage the records of the tile's rows (4 words per hash) and find
-        // the key envelope: lo_t(i) is non-decreasing in i, so the first row
-        // bounds it from the left (the last row from the right)
-        const int w0 = i0 >> 5;
-        const int ilast = min(i0 + BM - 1, n - 1);
+        // records of both tiles' rows (4 words per hash); lo_t(i) is
+        // non-decreasing in i, so a tile's first row bounds the envelope from
+        // the left (its last row from the right)
         int mylo = INT_MAX, myhi = 0;
-        uint4* dst = stage + slot * s * kWordsPerTile;
-        for (int e = lane; e < s * kWordsPerTile; e += 32) {
-          const int t = e / kWordsPerTile, wq = e % kWordsPerTile;
-          const int wd = min(w0 + wq, (int)a.W - 1);
-          const uint4 rv = __ldg(reinterpret_cast<const uint4*>(a.rec) +
-                                 ((int64_t)h * s + t) * a.W + wd);
-          dst[e] = rv;
-          const BinRecord rc = unpack_record(rv);
-          if (wq == 0) mylo = min(mylo, bin_lo(rc, i0));
-          if (!CAUSAL && wd == (ilast >> 5)) myhi = max(myhi, bin_hi(rc, ilast));
+        const int per = s * kWordsPerTile;
+        uint4 rv[4];
+        int ecount = 0;
+#pragma unroll 1
+        for (int e0 = 0; e0 < 2 * per; e0 += 4 * 32) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int e = e0 + u * 32 + lane;
+            if (e < 2 * per) {
+              const int tile = e / per, el = e % per;
+              const int qt = tile ? qtB : qtA;
+              const int h = tile ? hB : hA;
+              const int t = el / kWordsPerTile, wq = el % kWordsPerTile;
+              const int wd = min((max(qt, 0) * BM >> 5) + wq, (int)a.W - 1);
+              rv[u] = __ldg(reinterpret_cast<const uint4*>(a.rec) +
+                            ((int64_t)h * s + t) * a.W + wd);
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int e = e0 + u * 32 + lane;
+            if (e < 2 * per) {
+              const int tile = e / per, el = e % per;
+              const int qt = tile ? qtB : qtA;
+              stage[(slot * 2 + tile) * per + el] = rv[u];
+              if (qt < 0) continue;
+              const int i0 = qt * BM;
+              const int ilast = min(i0 + BM - 1, n - 1);
+              const int wq = el % kWordsPerTile;
+              const BinRecord rc = unpack_record(rv[u]);
+              if (wq == 0) mylo = min(mylo, bin_lo(rc, i0));
+              if (!CAUSAL && min((i0 >> 5) + wq, (int)a.W - 1) == (ilast >> 5))
+                myhi = max(myhi, bin_hi(rc, ilast));
+            }
+          }
+          ecount += 4 * 32;
         }
         mylo = __reduce_min_sync(FULL, mylo);
         kt_lo = mylo / BN;
         if (CAUSAL) {
-          kt_hi = qt + 1;
+          kt_hi = qmax + 1;
         } else {
           myhi = __reduce_max_sync(FULL, myhi);
           kt_hi = (myhi + BN - 1) / BN;
         }
         __syncwarp();
       }
-      kt_lo = min(kt_lo, qt);
+      kt_lo = min(kt_lo, qmax);
       kt_hi = max(kt_hi, kt_lo + 1);
       if (lane == 0) {
         volatile int* it = reinterpret_cast<volatile int*>(&ctl->ring[slot]);
-        it[0] = 1; it[1] = b; it[2] = h; it[3] = qt; it[4] = kt_lo; it[5] = kt_hi;
+        it[0] = 1; it[1] = b; it[2] = hA; it[3] = hB; it[4] = qtA; it[5] = qtB;
+        it[6] = kt_lo; it[7] = kt_hi;
         mbar_arrive(bar(B_IFULL + slot));
-        const int qs = seq & 1;
-        ok = mbar_wait(bar(B_QEMPTY + qs), (use & 1u) ^ 1u, abort, lim);
-        if (ok) {
-          const int qp = b * Hq + h;
-          const uint32_t qdst = sbase + OFF_Q + qs * kTileBytes;
-          mbar_arrive_expect_tx(bar(B_QFULL + qs), kTileBytes);
-          tma_load_3d(qdst, &tmQ, bar(B_QFULL + qs), 0, i0, qp);
-          tma_load_3d(qdst + kHalfBytes, &tmQ, bar(B_QFULL + qs), 64, i0, qp);
-          ++q_issued[qs];
-        }
-        const int kvp = b * Hkv + h / (Hq / Hkv);
-        for (int kt = kt_hi - 1; ok && kt >= kt_lo; --kt, ++g) {
-          const int st = g & 1;
-          const uint32_t u = (uint32_t)g >> 1;
-          ok = mbar_wait(bar(B_KEMPTY + st), (u & 1u) ^ 1u, abort, lim);
-          if (!ok) break;
-          const uint32_t kdst = sbase + OFF_K + st * kTileBytes;
-          mbar_arrive_expect_tx(bar(B_KFULL + st), kTileBytes);
-          tma_load_3d(kdst, &tmK, bar(B_KFULL + st), 0, kt * BN, kvp);
-          tma_load_3d(kdst + kHalfBytes, &tmK, bar(B_KFULL + st), 64, kt * BN, kvp);
-          ++k_issued[st];
-          ok = mbar_wait(bar(B_VEMPTY + st), (u & 1u) ^ 1u, abort, lim);
-          if (!ok) break;
-          const uint32_t vdst = sbase + OFF_V + st * kTileBytes;
-          mbar_arrive_expect_tx(bar(B_VFULL + st), kTileBytes);
-          tma_load_3d(vdst, &tmV, bar(B_VFULL + st), 0, kt * BN, kvp);
-          tma_load_3d(vdst + kHalfBytes, &tmV, bar(B_VFULL + st), 64, kt * BN, kvp);
-          ++v_issued[st];
-        }
       }
-      ok = __shfl_sync(FULL, (int)ok, 0) != 0;
-      g = __shfl_sync(FULL, g, 0);
-      if (!ok) break;
+      __syncwarp();
     }
+    if (!ok && lane == 0) {
+      *abort = 1;
+      atomicOr(a.err, 1);
+    }
+    __syncwarp();
+  } else if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
     if (lane == 0) {
+      int ld = 0;                       // K/V loads issued (K and V alternate)
+      int q_issued = 0;
+      int kv_issued[kSlots] = {0, 0, 0};
+      bool ok = true;
+      for (int seq = 0; ok; ++seq) {
+        const int slot = seq % kRing;
+        const uint32_t use = (uint32_t)(seq / kRing);
+        ok = mbar_wait(bar(B_IFULL + slot), use & 1u, abort, lim);
+        if (!ok) break;
+        const Item it = read_item(ctl, slot);
+        if (!it.valid) break;
+        for (int tile = 0; tile < 2 && ok; ++tile) {
+          ok = mbar_wait(bar(B_QEMPTY + tile), ((uint32_t)seq & 1u) ^ 1u, abort, lim);
+          if (!ok) break;
+          // an unused tile B reloads A's rows so its scores stay finite
+          const int qt = (tile && it.qtB >= 0) ? it.qtB : it.qtA;
+          const int h = (tile && it.qtB >= 0) ? it.hB : it.hA;
+          const uint32_t qdst = sbase + OFF_Q + tile * kTileBytes;
+          mbar_arrive_expect_tx(bar(B_QFULL + tile), kTileBytes);
+          tma_load_3d(qdst, &tmQ, bar(B_QFULL + tile), 0, qt * BM, it.b * Hq + h);
+          tma_load_3d(qdst + kHalfBytes, &tmQ, bar(B_QFULL + tile), 64, qt * BM, it.b * Hq + h);
+        }
+        if (!ok) break;
+        ++q_issued;
+        const int kvp = it.b * Hkv + it.hA / (Hq / Hkv);
+        for (int kt = it.kt_hi - 1; ok && kt >= it.kt_lo; --kt) {
+          for (int kv = 0; kv < 2 && ok; ++kv, ++ld) {
+            const int sl = ld % kSlots;
+            const uint32_t u = (uint32_t)(ld / kSlots);
+            ok = mbar_wait(bar(B_KVEMPTY + sl), (u & 1u) ^ 1u, abort, lim);
+            if (!ok) break;
+            const uint32_t dst = sbase + OFF_KV + sl * kTileBytes;
+            const CUtensorMap* m = kv ? &tmV : &tmK;
+            mbar_arrive_expect_tx(bar(B_KVFULL + sl), kTileBytes);
+            tma_load_3d(dst, m, bar(B_KVFULL + sl), 0, kt * BN, kvp);
+            tma_load_3d(dst + kHalfBytes, m, bar(B_KVFULL + sl), 64, kt * BN, kvp);
+            ++kv_issued[sl];
+          }
+        }
+        if (ok) mbar_arrive(bar(B_IEMPTY + slot));
+      }
       if (!ok) {
         *abort = 1;
         atomicOr(a.err, 1);
       }
       // let every copy this warp started land before the CTA can exit
-      for (int st = 0; st < 2; ++st) {
-        if (q_issued[st])
-          mbar_wait(bar(B_QFULL + st), (uint32_t)(q_issued[st] - 1) & 1u, nullptr, lim);
-        if (k_issued[st])
-          mbar_wait(bar(B_KFULL + st), (uint32_t)(k_issued[st] - 1) & 1u, nullptr, lim);
-        if (v_issued[st])
-          mbar_wait(bar(B_VFULL + st), (uint32_t)(v_issued[st] - 1) & 1u, nullptr, lim);
+      if (q_issued) {
+        mbar_wait(bar(B_QFULL + 0), (uint32_t)(q_issued - 1) & 1u, nullptr, lim);
+        mbar_wait(bar(B_QFULL + 1), (uint32_t)(q_issued - 1) & 1u, nullptr, lim);
       }
+      for (int sl = 0; sl < kSlots; ++sl)
+        if (kv_issued[sl])
+          mbar_wait(bar(B_KVFULL + sl), (uint32_t)(kv_issued[sl] - 1) & 1u, nullptr, lim);
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, 0, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, HD, 0, 1);
       bool ok = true;
-      int g = 0;
-      auto issue_pv = [&](int gp, bool first) -> bool {
-        const int st = gp & 1;
-        const uint32_t u = (uint32_t)gp >> 1;
-        if (!mbar_wait(bar(B_PFULL), (uint32_t)gp & 1u, abort, lim)) return false;
-        if (!mbar_wait(bar(B_VFULL + st), u & 1u, abort, lim)) return false;
-        tc_fence_after();
-        const uint32_t vbase = sbase + OFF_V + st * kTileBytes;
+      int ld = 0;        // K/V loads consumed so far (same numbering as producer)
+      int gt = 0;        // tiles processed so far (both tiles advance together)
+      auto wait_slot = [&](int l) -> bool {
+        return mbar_wait(bar(B_KVFULL + l % kSlots), (uint32_t)(l / kSlots) & 1u, abort, lim);
+      };
+      auto issue_s = [&](int tile, int lk) {
+        const uint32_t qbase = sbase + OFF_Q + tile * kTileBytes;
+        const uint32_t kbase = sbase + OFF_KV + (lk % kSlots) * kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint32_t koff = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+          mma_bf16_ss(tmem + tile * BN, desc_sw128(qbase + koff, 16, 1024),
+                      desc_sw128(kbase + koff, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(B_SFULL + tile));
+      };
+      auto issue_pv = [&](int tile, int lv, bool first) {
+        const uint32_t vbase = sbase + OFF_KV + (lv % kSlots) * kTileBytes;
         // keys 16kk..16kk+15 sit in chunk kk/2: P_hi in its first 16
         // columns, P_lo in the next 16, 8 packed columns per 16 keys
-        const uint32_t pcol = tmem + st * BN;
+        const uint32_t pcol = tmem + tile * BN;
+        const uint32_t ocol = tmem + kColO + tile * HD;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
           const uint64_t bd = desc_sw128(vbase + kk * 2048, kHalfBytes, 1024);
           const uint32_t ac = pcol + (kk >> 1) * 32 + (kk & 1) * 8;
-          mma_bf16_ts(tmem + kColO, ac, bd, idesc_pv, (first && kk == 0) ? 0u : 1u);
-          mma_bf16_ts(tmem + kColO, ac + 16, bd, idesc_pv, 1u);
+          mma_bf16_ts(ocol, ac, bd, idesc_pv, (first && kk == 0) ? 0u : 1u);
+          mma_bf16_ts(ocol, ac + 16, bd, idesc_pv, 1u);
         }
-        mma_commit(bar(B_PVDONE));
-        mma_commit(bar(B_VEMPTY + st));
-        return true;
       };
-      for (int seq = 0; ok; ++seq) {
-        const int slot = seq & 1;
-        const uint32_t use = (uint32_t)seq >> 1;
-        ok = mbar_wait(bar(B_IFULL + slot), use & 1u, abort, lim);
-        if (!ok) break;
-        const Item it = read_item(ctl, slot);
-        if (!it.valid) break;
-        const int ntiles = it.kt_hi - it.kt_lo;
-        const int qs = seq & 1;
-        ok = mbar_wait(bar(B_QFULL + qs), use & 1u, abort, lim);
-        if (!ok) break;
-        const uint32_t qbase = sbase + OFF_Q + qs * kTileBytes;
-        for (int jj = 0; jj < ntiles; ++jj, ++g) {
-          const int st = g & 1;
-          const uint32_t u = (uint32_t)g >> 1;
-          ok = mbar_wait(bar(B_KFULL + st), u & 1u, abort, lim);
+      // one continuous stream of tiles across items: the head of an item
+      // (its first S_A, S_B) is issued between the tail P Vs of the item
+      // before, so that Q loads and epilogues overlap tensor work
+      int seq = 0;
+      ok = mbar_wait(bar(B_IFULL + 0), 0u, abort, lim);
+      Item cur = ok ? read_item(ctl, 0) : Item{0, 0, 0, 0, 0, 0, 0, 0};
+      int T = cur.kt_hi - cur.kt_lo, jj = 0;
+      bool have_prev = false;
+      int prev_lv = 0, prev_slot = 0;
+      bool prev_first = false, prev_last = false;
+      while (ok && cur.valid) {
+        const int lk = ld;                      // K of this tile; V is ld + 1
+        if (have_prev) {
+          ok = mbar_wait(bar(B_PFULL + 0), (uint32_t)(gt - 1) & 1u, abort, lim) &&
+               wait_slot(prev_lv);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t kbase = sbase + OFF_K + st * kTileBytes;
-#pragma unroll
-          for (int kk = 0; kk < HD / 16; ++kk) {
-            const uint32_t koff = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-            const uint64_t ad = desc_sw128(qbase + koff, 16, 1024);
-            const uint64_t bd = desc_sw128(kbase + koff, 16, 1024);
-            mma_bf16_ss(tmem + st * BN, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(bar(B_SFULL + st));
-          mma_commit(bar(B_KEMPTY + st));
-          if (jj == ntiles - 1) mma_commit(bar(B_QEMPTY + qs));
-          if (jj > 0) {
-            ok = issue_pv(g - 1, jj == 1);
-            if (!ok) break;
+          issue_pv(0, prev_lv, prev_first);
+          if (prev_last) mma_commit(bar(B_ODONE + 0));
+        }
+        ok = wait_slot(lk);
+        if (!ok) break;
+        if (jj == 0) {
+          ok = mbar_wait(bar(B_QFULL + 0), (uint32_t)seq & 1u, abort, lim);
+          if (!ok) break;
+        }
+        tc_fence_after();
+        issue_s(0, lk);
+        if (jj == T - 1) mma_commit(bar(B_QEMPTY + 0));
+        if (have_prev) {
+          ok = mbar_wait(bar(B_PFULL + 1), (uint32_t)(gt - 1) & 1u, abort, lim);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(1, prev_lv, prev_first);
+          mma_commit(bar(B_KVEMPTY + prev_lv % kSlots));
+          if (prev_last) {
+            mma_commit(bar(B_ODONE + 1));
+            mbar_arrive(bar(B_IEMPTY + prev_slot));
           }
         }
-        if (!ok) break;
-        ok = issue_pv(g - 1, ntiles == 1);
-        if (!ok) break;
-        mbar_arrive(bar(B_IEMPTY + slot));
+        if (jj == 0) {
+          ok = mbar_wait(bar(B_QFULL + 1), (uint32_t)seq & 1u, abort, lim);
+          if (!ok) break;
+        }
+        tc_fence_after();
+        issue_s(1, lk);
+        mma_commit(bar(B_KVEMPTY + lk % kSlots));
+        if (jj == T - 1) mma_commit(bar(B_QEMPTY + 1));
+        have_prev = true;
+        prev_lv = lk + 1;
+        prev_first = jj == 0;
+        prev_last = jj == T - 1;
+        prev_slot = seq % kRing;
+        ld += 2;
+        ++gt;
+        if (++jj == T) {
+          ++seq;
+          ok = mbar_wait(bar(B_IFULL + seq % kRing), (uint32_t)(seq / kRing) & 1u, abort, lim);
+          if (!ok) break;
+          cur = read_item(ctl, seq % kRing);
+          T = cur.kt_hi - cur.kt_lo;
+          jj = 0;
+        }
+      }
+      if (ok && have_prev) {
+        // tail of the last tile
+        ok = mbar_wait(bar(B_PFULL + 0), (uint32_t)(gt - 1) & 1u, abort, lim) &&
+             wait_slot(prev_lv);
+        if (ok) {
+          tc_fence_after();
+          issue_pv(0, prev_lv, prev_first);
+          mma_commit(bar(B_ODONE + 0));
+          ok = mbar_wait(bar(B_PFULL + 1), (uint32_t)(gt - 1) & 1u, abort, lim);
+        }
+        if (ok) {
+          tc_fence_after();
+          issue_pv(1, prev_lv, prev_first);
+          mma_commit(bar(B_KVEMPTY + prev_lv % kSlots));
+          mma_commit(bar(B_ODONE + 1));
+          mbar_arrive(bar(B_IEMPTY + prev_slot));
+        }
       }
       if (!ok) {
         *abort = 1;
@@ -383,35 +527,66 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
     __syncwarp();
   } else {
     // ----------------------------------------------------- softmax / epilogue
-    const int r = threadIdx.x;   // row within the tile == TMEM lane
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const int tile = warp >> 2;                 // 0: tile A, 1: tile B
+    const int r = threadIdx.x & (BM - 1);       // row within the tile == TMEM lane
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t s_col = tmem + lane_base + tile * BN;
+    const uint32_t o_col = tmem + lane_base + kColO + tile * HD;
     const float scale_log2 = 1.4426950408889634f * 0.08838834764831845f;  // log2(e)/sqrt(128)
-    int* bpl = bp;                 // sorted bin starts of this row, [s][BM]
-    int* bph = bp + s * BM;        // sorted bin ends (non-causal), [s][BM]
+    const uint64_t scale2 = f2_pack(scale_log2, scale_log2);
+    const int nlists = CAUSAL ? 1 : 2;
+    int* bpl = bp + tile * nlists * s * BM;      // sorted bin starts, [s][BM]
+    int* bph = bpl + s * BM;                     // sorted bin ends (non-causal)
     bool ok = true;
     int g = 0;
     for (int seq = 0; ok; ++seq) {
-      const int slot = seq & 1;
-      const uint32_t use = (uint32_t)seq >> 1;
+      const int slot = seq % kRing;
+      const uint32_t use = (uint32_t)(seq / kRing);
       ok = __all_sync(FULL, mbar_wait(bar(B_IFULL + slot), use & 1u, abort, lim));
       if (!ok) break;
       const Item it = read_item(ctl, slot);
       if (!it.valid) break;
-      const int i0 = it.qt * BM;
+      const int qt = tile ? it.qtB : it.qtA;
+      const int h = tile ? it.hB : it.hA;
+      const int i0 = max(qt, 0) * BM;
       const int i = i0 + r;
-      const bool row_ok = i < n;
-      const int ii = row_ok ? i : n - 1;
-      const int h = it.h;
+      const bool row_ok = qt >= 0 && i < n;
+      const int ii = min(i, n - 1);
       const int ntiles = it.kt_hi - it.kt_lo;
       // keys that take part: [vlo, vhi]
       int vlo = 0, vhi = CAUSAL ? ii : n - 1;
       int pl = s, ph = s, ql = s, qh = s;
       float slope = 0.f;
+      int lo_r[SREG > 0 ? SREG : 1], hi_r[SREG > 0 ? SREG : 1];
+      int lomax = 0, himin = 0;
       if (EXACT) {
         slope = p.slope_log2[h];
-      } else {
+      } else if (SREG > 0) {
+        // this row's bin starts (and ends) under every hash, in registers
+        const uint4* rs = stage + (slot * 2 + tile) * s * kWordsPerTile + ((ii >> 5) - (i0 >> 5));
+        int lomin = INT_MAX, himax = 0;
+        lomax = INT_MIN;
+        himin = INT_MAX;
+#pragma unroll
+        for (int t = 0; t < (SREG > 0 ? SREG : 1); ++t) {
+          int lo = INT_MAX, hi = INT_MAX;
+          if (t < s) {
+            const BinRecord rc = unpack_record(rs[t * kWordsPerTile]);
+            lo = bin_lo(rc, ii);
+            hi = bin_hi(rc, ii);
+            lomin = min(lomin, lo);
+            lomax = max(lomax, lo);
+            himax = max(himax, hi);
+            himin = min(himin, hi);
+          }
+          lo_r[t] = lo;
+          hi_r[t] = hi;
+        }
+        vlo = lomin;
+        if (!CAUSAL) vhi = himax - 1;
+      } else if (qt >= 0) {
         // this row's bin starts (and ends) under every hash, sorted
-        const uint4* rs = stage + slot * s * kWordsPerTile + ((ii >> 5) - (i0 >> 5));
+        const uint4* rs = stage + (slot * 2 + tile) * s * kWordsPerTile + ((ii >> 5) - (i0 >> 5));
         for (int t = 0; t < s; ++t) {
           const BinRecord rc = unpack_record(rs[t * kWordsPerTile]);
           const int lo = bin_lo(rc, ii);
@@ -438,19 +613,21 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         vlo = bpl[r];
         if (!CAUSAL) vhi = bph[(s - 1) * BM + r] - 1;
       }
+      // e * slope for e = 0..31 in packed pairs (exact mode bias)
+      uint64_t eslope[16];
+#pragma unroll
+      for (int e2 = 0; e2 < 16; ++e2)
+        eslope[e2] = f2_pack((float)(2 * e2) * slope, (float)(2 * e2 + 1) * slope);
       float m_ref = -INFINITY, l = 0.f;
       for (int jj = 0; jj < ntiles; ++jj, ++g) {
-        const int st = g & 1;
-        const uint32_t u = (uint32_t)g >> 1;
         const int jt = (it.kt_hi - 1 - jj) * BN;
-        const uint32_t s_col = tmem + lane_base + st * BN;
-        ok = __all_sync(FULL, mbar_wait(bar(B_SFULL + st), u & 1u, abort, lim));
+        ok = __all_sync(FULL, mbar_wait(bar(B_SFULL + tile), (uint32_t)g & 1u, abort, lim));
         if (!ok) break;
         tc_fence_after();
 
         // pass 1: running max (log2 units) over the keys that take part
-        float mt = -INFINITY;
-#pragma unroll 1
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
         for (int q2 = 0; q2 < 2; ++q2) {
           uint32_t ra[32], rb2[32];
           tmem_ld32(s_col + q2 * 64, ra);
@@ -460,38 +637,41 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
           for (int half = 0; half < 2; ++half) {
             const uint32_t* rr = half ? rb2 : ra;
             const int jc = jt + q2 * 64 + half * 32;
+            float xv[32];
+            uint32_t vm;
             if (EXACT) {
               const float d0 = (float)(i - jc);
-              if (CAUSAL) {
-                const float base = -d0 * slope;
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                  float x = fmaf(__uint_as_float(rr[e]), scale_log2, fmaf((float)e, slope, base));
-                  if (jc + e > i) x = -INFINITY;
-                  mt = fmaxf(mt, x);
-                }
-              } else {
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                  float x = fmaf(__uint_as_float(rr[e]), scale_log2,
-                                 -fabsf(d0 - (float)e) * slope);
-                  if (jc + e >= n) x = -INFINITY;
-                  mt = fmaxf(mt, x);
+              for (int e = 0; e < 32; e += 2) {
+                if (CAUSAL) {
+                  const uint64_t b2 = f2_add(eslope[e >> 1], f2_pack(-d0 * slope, -d0 * slope));
+                  f2_unpack(f2_fma(f2_pack(__uint_as_float(rr[e]), __uint_as_float(rr[e + 1])),
+                                   scale2, b2), xv[e], xv[e + 1]);
+                } else {
+                  xv[e] = fmaf(__uint_as_float(rr[e]), scale_log2, -fabsf(d0 - (float)e) * slope);
+                  xv[e + 1] = fmaf(__uint_as_float(rr[e + 1]), scale_log2,
+                                   -fabsf(d0 - (float)(e + 1)) * slope);
                 }
               }
+              vm = key_mask(-1, CAUSAL ? i - jc : n - 1 - jc, row_ok);
             } else {
-              const int ea = vlo - jc, eb = vhi - jc;
-              if (__all_sync(FULL, ea <= 0 && eb >= 31)) {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) mt = fmaxf(mt, __uint_as_float(rr[e]));
-              } else {
+              for (int e = 0; e < 32; ++e) xv[e] = __uint_as_float(rr[e]);
+              vm = key_mask(vlo - jc, vhi - jc, row_ok);
+            }
+            if (__any_sync(FULL, vm != 0xffffffffu)) {
 #pragma unroll
-                for (int e = 0; e < 32; ++e)
-                  if (e >= ea && e <= eb) mt = fmaxf(mt, __uint_as_float(rr[e]));
-              }
+              for (int e = 0; e < 32; ++e)
+                if (!(vm & (1u << e))) xv[e] = -INFINITY;
+            }
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+              mx0 = max3(mx0, xv[e], xv[e + 1]);
+              mx1 = max3(mx1, xv[e + 2], xv[e + 3]);
             }
           }
         }
+        float mt = fmaxf(mx0, mx1);
         if (!EXACT) mt *= scale_log2;
         if (!row_ok) mt = -INFINITY;
         const float m_new = fmaxf(m_ref, mt);
@@ -500,65 +680,93 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         const float alpha = resc ? ex2(m_ref - m_new) : 1.f;
         const float mu = (m_use == -INFINITY || !row_ok) ? 0.f : m_use;
 
+        // a grown max rescales O; the commit behind S(g) proves P V(g-1) landed
+        if (jj > 0 && __any_sync(FULL, resc)) {
+          const float f = resc ? alpha : 1.f;
+#pragma unroll 1
+          for (int q = 0; q < 4; ++q) {
+            uint32_t o[32];
+            tmem_ld32(o_col + q * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+            tmem_st32(o_col + q * 32, o);
+          }
+        }
+
         // pass 2: P = c 2^(x - m) = P_hi + P_lo (two bf16 terms) written over
         // the chunk's own score columns; chunks in descending key order so
         // that the breakpoint pointers only move down
-        float lsum = 0.f;
+        uint64_t lsum2 = f2_pack(0.f, 0.f);
 #pragma unroll 1
         for (int q = 3; q >= 0; --q) {
           const int jc = jt + q * 32;
           uint32_t rr[32];
           tmem_ld32(s_col + q * 32, rr);
-          float pv[32];
+          int base = 0;
+          bool flat = true, big = false;
+          uint32_t up[5] = {0u, 0u, 0u, 0u, 0u}, dn[5] = {0u, 0u, 0u, 0u, 0u};
+          uint32_t vm;
           if (EXACT) {
-            tmem_wait_ld();
-            const float d0 = (float)(i - jc);
+            vm = key_mask(-1, CAUSAL ? i - jc : n - 1 - jc, row_ok);
+          } else if (SREG > 0) {
+            vm = key_mask(vlo - jc, vhi - jc, row_ok);
+            // rows past every bin start of the chunk (and before every end)
+            // have c = s throughout; otherwise count the registers
+            const bool deep = lomax <= jc && (CAUSAL || himin > jc + 31);
+            if (__all_sync(FULL, deep || vm == 0u)) {
+              base = s;
+            } else {
+              bool any = false;
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              float x = CAUSAL
-                  ? fmaf(__uint_as_float(rr[e]), scale_log2, fmaf((float)e, slope, -d0 * slope))
-                  : fmaf(__uint_as_float(rr[e]), scale_log2, -fabsf(d0 - (float)e) * slope);
-              if (CAUSAL ? (jc + e > i) : (jc + e >= n)) x = -INFINITY;
-              pv[e] = ex2(x - mu);
+              for (int t = 0; t < (SREG > 0 ? SREG : 1); ++t) {
+                const int dl = lo_r[t] - jc;
+                base += dl <= 0 ? 1 : 0;
+                any = any || (unsigned)(dl - 1) < 31u;
+                if (!CAUSAL) {
+                  const int dh = hi_r[t] - jc;
+                  base -= dh <= 0 ? 1 : 0;
+                  any = any || (unsigned)(dh - 1) < 31u;
+                }
+              }
+              flat = !any || vm == 0u;
+              if (__any_sync(FULL, !flat)) {
+#pragma unroll
+                for (int t = 0; t < (SREG > 0 ? SREG : 1); ++t) {
+                  const int dl = lo_r[t] - jc;
+                  plane_add(up, (unsigned)(dl - 1) < 31u ? (1u << dl) : 0u);
+                  if (!CAUSAL) {
+                    const int dh = hi_r[t] - jc;
+                    plane_add(dn, (unsigned)(dh - 1) < 31u ? (1u << dh) : 0u);
+                  }
+                }
+              }
             }
           } else {
+            vm = key_mask(vlo - jc, vhi - jc, row_ok);
             while (pl > 0 && bpl[(pl - 1) * BM + r] > jc) --pl;
             while (ph > pl && bpl[(ph - 1) * BM + r] > jc + 31) --ph;
-            int base = pl;
-            bool flat = ph == pl;
+            base = pl;
+            flat = ph == pl;
             if (!CAUSAL) {
               while (ql > 0 && bph[(ql - 1) * BM + r] > jc) --ql;
               while (qh > ql && bph[(qh - 1) * BM + r] > jc + 31) --qh;
               base -= ql;
               flat = flat && qh == ql;
             }
-            const int ea = vlo - jc, eb = vhi - jc;
-            const bool inside = ea <= 0 && eb >= 31 && row_ok;
-            const bool outside = ea > 31 || eb < 0 || !row_ok;
-            tmem_wait_ld();
-            if (__all_sync(FULL, outside)) {
-#pragma unroll
-              for (int e = 0; e < 32; ++e) pv[e] = 0.f;
-            } else if (__all_sync(FULL, (flat && inside) || outside)) {
-              // one multiplicity for the whole chunk: log2(c) rides in the FMA
-              const float off = outside ? -INFINITY : lg2((float)base) - mu;
-#pragma unroll
-              for (int e = 0; e < 32; ++e)
-                pv[e] = ex2(fmaf(__uint_as_float(rr[e]), scale_log2, off));
-            } else {
-              float cf[32];
-#pragma unroll
-              for (int e = 0; e < 32; ++e) cf[e] = (float)base;
-              // one ramp per distinct step position inside the chunk
+            if (vm == 0u) flat = true;
+            if (!flat) {
+              // binary planes of the step multiplicities inside the chunk
               for (int k = pl; k < ph;) {
                 const int bpos = bpl[k * BM + r];
                 int k2 = k + 1;
                 while (k2 < ph && bpl[k2 * BM + r] == bpos) ++k2;
-                const int bo = bpos - jc;
-                const float mult = (float)(k2 - k);
+                const uint32_t bit = 1u << (bpos - jc);
+                const int m = k2 - k;
 #pragma unroll
-                for (int e = 0; e < 32; ++e)
-                  if (e >= bo) cf[e] += mult;
+                for (int b = 0; b < 5; ++b)
+                  if (m & (1 << b)) up[b] |= bit;
+                big = big || m >= 32;
                 k = k2;
               }
               if (!CAUSAL) {
@@ -566,85 +774,140 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                   const int bpos = bph[k * BM + r];
                   int k2 = k + 1;
                   while (k2 < qh && bph[k2 * BM + r] == bpos) ++k2;
-                  const int bo = bpos - jc;
-                  const float mult = (float)(k2 - k);
+                  const uint32_t bit = 1u << (bpos - jc);
+                  const int m = k2 - k;
 #pragma unroll
-                  for (int e = 0; e < 32; ++e)
-                    if (e >= bo) cf[e] -= mult;
+                  for (int b = 0; b < 5; ++b)
+                    if (m & (1 << b)) dn[b] |= bit;
+                  big = big || m >= 32;
                   k = k2;
                 }
               }
-#pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                const bool in = e >= ea && e <= eb && row_ok;
-                pv[e] = in ? ex2(fmaf(__uint_as_float(rr[e]), scale_log2, -mu)) * cf[e] : 0.f;
-              }
             }
           }
+          tmem_wait_ld();
           uint32_t hi[16], lo[16];
+          if (__all_sync(FULL, vm == 0u)) {
 #pragma unroll
-          for (int e2 = 0; e2 < 16; ++e2) {
-            const float p0 = pv[2 * e2], p1 = pv[2 * e2 + 1];
-            lsum += p0 + p1;
-            const uint32_t hp = pack_bf16(p0, p1);
-            hi[e2] = hp;
-            lo[e2] = pack_bf16(p0 - __uint_as_float(hp << 16),
-                               p1 - __uint_as_float(hp & 0xffff0000u));
+            for (int e2 = 0; e2 < 16; ++e2) { hi[e2] = 0u; lo[e2] = 0u; }
+          } else {
+            const bool all_flat = EXACT || __all_sync(FULL, flat);
+            float off;
+            if (EXACT) off = -(float)(i - jc) * slope - mu;
+            else off = (all_flat ? lg2((float)max(base, 1)) : 0.f) - mu;
+            float pv[32];
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              uint64_t b2 = f2_pack(off, off);
+              if (EXACT && CAUSAL) b2 = f2_add(eslope[e >> 1], b2);
+              uint64_t a2;
+              if (EXACT && !CAUSAL) {
+                const float d0 = (float)(i - jc);
+                a2 = f2_pack(fmaf(__uint_as_float(rr[e]), scale_log2,
+                                  -fabsf(d0 - (float)e) * slope - mu),
+                             fmaf(__uint_as_float(rr[e + 1]), scale_log2,
+                                  -fabsf(d0 - (float)(e + 1)) * slope - mu));
+              } else {
+                a2 = f2_fma(f2_pack(__uint_as_float(rr[e]), __uint_as_float(rr[e + 1])),
+                            scale2, b2);
+              }
+              f2_unpack(a2, pv[e], pv[e + 1]);
+            }
+            if (__any_sync(FULL, vm != 0xffffffffu)) {
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                if (!(vm & (1u << e))) pv[e] = -INFINITY;
+            }
+#pragma unroll
+            for (int e = 0; e < 32; ++e) pv[e] = ex2(pv[e]);
+            if (!EXACT && !all_flat) {
+              // c_ij inside the chunk: a running count of the bin starts
+              // (minus bin ends), one plane per bit of the multiplicities
+              const float fb = (float)base;
+              if (__any_sync(FULL, big)) {
+                float cf[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) cf[e] = fb;
+                for (int k = pl; k < ph; ++k) {
+                  const int bo = bpl[k * BM + r] - jc;
+#pragma unroll
+                  for (int e = 0; e < 32; ++e)
+                    if (e >= bo) cf[e] += 1.f;
+                }
+                if (!CAUSAL) {
+                  for (int k = ql; k < qh; ++k) {
+                    const int bo = bph[k * BM + r] - jc;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                      if (e >= bo) cf[e] -= 1.f;
+                  }
+                }
+#pragma unroll
+                for (int e = 0; e < 32; ++e) pv[e] *= cf[e];
+              } else if (__any_sync(FULL, (up[4] | dn[4]) != 0u)) {
+                scale_by_count<5, CAUSAL>(pv, fb, up, dn);
+              } else if (__any_sync(FULL, (up[3] | dn[3]) != 0u)) {
+                scale_by_count<4, CAUSAL>(pv, fb, up, dn);
+              } else if (__any_sync(FULL, (up[2] | dn[2]) != 0u)) {
+                scale_by_count<3, CAUSAL>(pv, fb, up, dn);
+              } else if (__any_sync(FULL, (up[1] | dn[1]) != 0u)) {
+                scale_by_count<2, CAUSAL>(pv, fb, up, dn);
+              } else {
+                scale_by_count<1, CAUSAL>(pv, fb, up, dn);
+              }
+            }
+#pragma unroll
+            for (int e2 = 0; e2 < 16; ++e2) {
+              const uint64_t p2 = f2_pack(pv[2 * e2], pv[2 * e2 + 1]);
+              lsum2 = f2_add(lsum2, p2);
+              const uint32_t hp = pack_bf16(pv[2 * e2], pv[2 * e2 + 1]);
+              float l0, l1;
+              f2_unpack(f2_sub(p2, f2_pack(__uint_as_float(hp << 16),
+                                           __uint_as_float(hp & 0xffff0000u))), l0, l1);
+              hi[e2] = hp;
+              lo[e2] = pack_bf16(l0, l1);
+            }
           }
           tmem_st16(s_col + q * 32, hi);
           tmem_st16(s_col + q * 32 + 16, lo);
         }
-        l = l * alpha + lsum;
+        float ls0, ls1;
+        f2_unpack(lsum2, ls0, ls1);
+        l = l * alpha + (ls0 + ls1);
         m_ref = m_use;
-
-        // P(g) may be published once P V(g-1) has landed: this keeps every
-        // barrier within one phase of its waiters, and a grown max rescales
-        // O only after that product
-        if (g > 0) {
-          ok = __all_sync(FULL, mbar_wait(bar(B_PVDONE), (uint32_t)(g - 1) & 1u, abort, lim));
-          if (!ok) break;
-        }
-        tc_fence_after();
-        if (jj > 0 && __any_sync(FULL, resc)) {
-          const float f = resc ? alpha : 1.f;
-#pragma unroll 1
-          for (int q = 0; q < 4; ++q) {
-            uint32_t o[32];
-            const uint32_t ta = tmem + lane_base + kColO + q * 32;
-            tmem_ld32(ta, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
-            tmem_st32(ta, o);
-          }
-        }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bar(B_PFULL));
+        mbar_arrive(bar(B_PFULL + tile));
       }
       if (!ok) break;
 
       // epilogue: O_i = acc_i / l_i
-      ok = __all_sync(FULL, mbar_wait(bar(B_PVDONE), (uint32_t)(g - 1) & 1u, abort, lim));
+      ok = __all_sync(FULL, mbar_wait(bar(B_ODONE + tile), (uint32_t)seq & 1u, abort, lim));
       if (!ok) break;
       tc_fence_after();
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
       uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.O) +
                                              (((int64_t)it.b * Hq + h) * n + ii) * HD);
-#pragma unroll 1
-      for (int q = 0; q < 4; ++q) {
-        uint32_t o[32];
-        tmem_ld32(tmem + lane_base + kColO + q * 32, o);
+#pragma unroll
+      for (int q2 = 0; q2 < 2; ++q2) {
+        uint32_t o0[32], o1[32];
+        tmem_ld32(o_col + q2 * 64, o0);
+        tmem_ld32(o_col + q2 * 64 + 32, o1);
         tmem_wait_ld();
-        uint32_t pk[16];
 #pragma unroll
-        for (int e2 = 0; e2 < 16; ++e2)
-          pk[e2] = pack_bf16(__uint_as_float(o[2 * e2]) * inv_l,
-                             __uint_as_float(o[2 * e2 + 1]) * inv_l);
-        if (row_ok) {
+        for (int half = 0; half < 2; ++half) {
+          const uint32_t* o = half ? o1 : o0;
+          uint32_t pk[16];
 #pragma unroll
-          for (int v = 0; v < 4; ++v)
-            orow[q * 4 + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          for (int e2 = 0; e2 < 16; ++e2)
+            pk[e2] = pack_bf16(__uint_as_float(o[2 * e2]) * inv_l,
+                               __uint_as_float(o[2 * e2 + 1]) * inv_l);
+          if (row_ok) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              orow[(q2 * 2 + half) * 4 + v] =
+                  make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          }
         }
       }
       tc_fence_before();
@@ -658,7 +921,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -710,11 +973,11 @@ bool make_map(CUtensorMap* map, const void* base, int64_t planes, int64_t n) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool EXACT, bool CAUSAL>
+template <bool EXACT, bool CAUSAL, int SREG>
 cudaError_t launch_variant(const CUtensorMap& mq, const CUtensorMap& mk,
                            const CUtensorMap& mv, const TcParams& p,
                            size_t smem, int grid, cudaStream_t st) {
-  auto kern = attn_tc_kernel<EXACT, CAUSAL>;
+  auto kern = attn_tc_kernel<EXACT, CAUSAL, SREG>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
@@ -724,8 +987,11 @@ cudaError_t launch_variant(const CUtensorMap& mq, const CUtensorMap& mk,
 
 }  // namespace
 
+constexpr int kSreg = 16;
+
 size_t attn_tc_smem_bytes(int s, int causal, int exact) {
-  return 1024 + OFF_BP + bp_bytes(s, exact != 0, causal != 0) +
+  const int sreg = (!exact && s <= kSreg) ? kSreg : 0;
+  return 1024 + OFF_BP + bp_bytes(s, exact != 0, causal != 0, sreg) +
          stage_bytes(s, exact != 0) + sizeof(Ctl);
 }
 
@@ -741,15 +1007,18 @@ cudaError_t launch_attn_tc(const AttnArgs& a, const float* slopes_host,
   for (int h = 0; h < 512; ++h)
     p.slope_log2[h] = (slopes_host && h < a.Hq) ? slopes_host[h] : 0.f;
   p.QT = (a.n + BM - 1) / BM;
-  p.num_items = a.B * a.Hq * p.QT;
-  const int grid = p.num_items < num_sms ? p.num_items : num_sms;
+  const int grid = a.num_items < num_sms ? a.num_items : num_sms;
   const size_t smem = attn_tc_smem_bytes(a.s, a.causal, a.exact);
   if (a.exact) {
-    return a.causal ? launch_variant<true, true>(mq, mk, mv, p, smem, grid, st)
-                    : launch_variant<true, false>(mq, mk, mv, p, smem, grid, st);
+    return a.causal ? launch_variant<true, true, 0>(mq, mk, mv, p, smem, grid, st)
+                    : launch_variant<true, false, 0>(mq, mk, mv, p, smem, grid, st);
   }
-  return a.causal ? launch_variant<false, true>(mq, mk, mv, p, smem, grid, st)
-                  : launch_variant<false, false>(mq, mk, mv, p, smem, grid, st);
+  if (a.s <= kSreg) {
+    return a.causal ? launch_variant<false, true, kSreg>(mq, mk, mv, p, smem, grid, st)
+                    : launch_variant<false, false, kSreg>(mq, mk, mv, p, smem, grid, st);
+  }
+  return a.causal ? launch_variant<false, true, 0>(mq, mk, mv, p, smem, grid, st)
+                  : launch_variant<false, false, 0>(mq, mk, mv, p, smem, grid, st);
 }
 
 }  // namespace plsh

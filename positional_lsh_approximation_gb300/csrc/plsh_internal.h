@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <map>
 #include <string>
 #include <vector>
 
@@ -25,6 +26,14 @@ constexpr int kMaxS = 64;
 constexpr int kMaxExactHeads = 512;
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 
+// Work-item table of the tensor-core kernel for one problem shape and head
+// order, kept on the device once built.
+struct ItemTable {
+  std::vector<int4> host;
+  int4* dev = nullptr;
+  uint64_t last_use = 0;
+};
+
 // Per-device library state.
 struct DeviceCtx {
   int device = -1;
@@ -33,7 +42,10 @@ struct DeviceCtx {
   int* d_queue = nullptr;      // kQueueSlots x {next item, finished CTAs}
   uint64_t slot_counter = 0;
   uint64_t wait_ns = kDefaultWaitNs;
+  std::map<std::string, ItemTable> tables;
+  uint64_t table_clock = 0;
 };
+constexpr size_t kMaxTables = 16;
 constexpr int kQueueSlots = 1024;
 
 }  // namespace plsh
@@ -72,7 +84,10 @@ struct AttnArgs {
   const BinRecord* rec;            // [Hq*s][W] (approximate mode)
   int s;
   int64_t W;
-  const int32_t* head_order;       // [Hq] (approximate mode)
+  // tensor-core path: work items, each two 128-row query tiles that share
+  // one KV head, {b, hA | hB << 16, qtA, qtB (-1: none)}, in cost order
+  const int4* items;
+  int num_items;
   int* err;
   int* queue;                      // {next item, finished CTAs}
   uint64_t wait_ns;

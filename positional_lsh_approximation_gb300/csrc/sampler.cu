@@ -20,6 +20,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "plsh_internal.h"
 
 namespace plsh {
@@ -64,74 +66,24 @@ __device__ double ln_rn(double x) {
     m = __dmul_rn(m, 0.5);
     e += 1;
   }
+  // 1/(2k+1), each the correctly rounded quotient (folded by the compiler)
+  constexpr double kInvOdd[12] = {1.0 / 1,  1.0 / 3,  1.0 / 5,  1.0 / 7,
+                                  1.0 / 9,  1.0 / 11, 1.0 / 13, 1.0 / 15,
+                                  1.0 / 17, 1.0 / 19, 1.0 / 21, 1.0 / 23};
   const double z = __ddiv_rn(__dadd_rn(m, -1.0), __dadd_rn(m, 1.0));
   const double z2 = __dmul_rn(z, z);
-  double poly = __ddiv_rn(1.0, 23.0);
+  double poly = kInvOdd[11];
 #pragma unroll
-  for (int k = 10; k >= 0; --k) {
-    poly = __dadd_rn(__dmul_rn(poly, z2), __ddiv_rn(1.0, (double)(2 * k + 1)));
-  }
+  for (int k = 10; k >= 0; --k) poly = __dadd_rn(__dmul_rn(poly, z2), kInvOdd[k]);
   const double ln_m = __dmul_rn(__dadd_rn(z, z), poly);
   const double ed = (double)e;
   return __dadd_rn(__dmul_rn(ed, kLn2Hi),
                    __dadd_rn(__dmul_rn(ed, kLn2Lo), ln_m));
 }
 
-__global__ void draw_kernel(const double* __restrict__ sigma, int H, int s,
-                            uint64_t seed, double* __restrict__ w_out,
-                            double* __restrict__ u_out) {
-  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= H * s) return;
-  const int h = idx / s, t = idx % s;
-  uint32_t c[4] = {(uint32_t)t, (uint32_t)h, 0u, 0u};
-  philox4x32_10(c, (uint32_t)(seed & 0xffffffffu), (uint32_t)(seed >> 32));
-  const double two_m32 = 0x1p-32;
-  const double u0 = __dmul_rn(__dadd_rn((double)c[0], 0.5), two_m32);
-  const double u1 = __dmul_rn(__dadd_rn((double)c[1], 0.5), two_m32);
-  const double u2 = __dmul_rn(__dadd_rn((double)c[2], 0.5), two_m32);
-  const double e0 = -ln_rn(u0);
-  const double e1 = -ln_rn(u1);
-  const double w = __dmul_rn(sigma[h], __dadd_rn(e0, e1));
-  w_out[idx] = w;
-  u_out[idx] = __dmul_rn(w, u2);
-}
-
 // ceil(u + k w) with the multiply and the add rounded separately.
 __device__ __forceinline__ double start_of(long long k, double w, double u) {
   return ceil(__dadd_rn(u, __dmul_rn((double)k, w)));
-}
-
-// Bitmap word `word` of hash `hs`: bit r set when position 32*word + r opens
-// a bin.  One thread per (hash, word).
-__global__ void bits_from_draws_kernel(int64_t n, int64_t W, int HS,
-                                       const double* __restrict__ w_in,
-                                       const double* __restrict__ u_in,
-                                       BinRecord* __restrict__ rec) {
-  const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (gid >= (int64_t)HS * W) return;
-  const int hs = (int)(gid / W);
-  const int64_t word = gid % W;
-  const double w = w_in[hs], u = u_in[hs];
-  const int64_t p0 = word * 32;
-  const int64_t p1 = (p0 + 32 < n) ? p0 + 32 : n;   // positions [p0, p1)
-  uint32_t bits = 0;
-  if (w < 1.0) {
-    const int64_t cnt = p1 - p0;
-    bits = cnt >= 32 ? 0xffffffffu : ((1u << cnt) - 1u);
-  } else {
-    if (p0 == 0) bits |= 1u;
-    // first k whose start can reach p0: k ~ (p0 - 1 - u) / w, stepped back two
-    // to absorb rounding, then walk forward over the exact starts.
-    double est = floor(((double)(p0 - 1) - u) / w) - 2.0;
-    long long k = est > 0.0 ? (long long)est : 0ll;
-    const double lim = (double)p1;
-    for (;; ++k) {
-      const double c = start_of(k, w, u);
-      if (c >= lim) break;
-      if (c >= (double)p0) bits |= 1u << ((int64_t)c - p0);
-    }
-  }
-  rec[gid].bits = bits;
 }
 
 // One thread per listed start (terminal entries excluded): set its bit.
@@ -222,16 +174,156 @@ prev_next_kernel(int64_t n, int64_t W, BinRecord* __restrict__ rec) {
   }
 }
 
+// The sampler, one CTA per (hash, segment of kSegWords words): the draw (two
+// threads, one logarithm each; every CTA of a hash computes the same bits),
+// the segment's bin starts set in a shared-memory bitmap (one thread per k,
+// start ceil(u + k w)), the last start before the segment and the first after
+// it taken from the same k walk, and the records from two block scans.
+constexpr int kSampThreads = 128;
+constexpr int kSegWords = 64;
+
+// Block-wide exclusive scan of `v` with operator max (fwd) or min (!fwd):
+// thread t receives the combination of threads before it (after it for !fwd)
+// and `ident` when there are none.  All threads must call it.
+__device__ __forceinline__ int32_t block_excl_scan(int32_t v, bool fwd, int32_t ident,
+                                                   int32_t* warp_buf) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  constexpr int nw = kSampThreads / 32;
+  int32_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t t = fwd ? __shfl_up_sync(0xffffffffu, incl, o)
+                          : __shfl_down_sync(0xffffffffu, incl, o);
+    const bool take = fwd ? lane >= o : lane + o < 32;
+    if (take) incl = fwd ? max(incl, t) : min(incl, t);
+  }
+  int32_t excl = fwd ? __shfl_up_sync(0xffffffffu, incl, 1)
+                     : __shfl_down_sync(0xffffffffu, incl, 1);
+  if (fwd ? lane == 0 : lane == 31) excl = ident;
+  if (fwd ? lane == 31 : lane == 0) warp_buf[wid] = incl;
+  __syncthreads();
+  int32_t before = ident;
+#pragma unroll
+  for (int q = 0; q < nw; ++q) {
+    if (fwd ? q < wid : q > wid)
+      before = fwd ? max(before, warp_buf[q]) : min(before, warp_buf[q]);
+  }
+  __syncthreads();
+  return fwd ? max(excl, before) : min(excl, before);
+}
+
+__global__ void __launch_bounds__(kSampThreads)
+sample_kernel(int64_t n, int64_t W, int nseg, int spc, int s,
+              const double* __restrict__ sigma, uint64_t seed,
+              double* __restrict__ w_out, double* __restrict__ u_out,
+              BinRecord* __restrict__ rec) {
+  const int cps = (nseg + spc - 1) / spc;      // CTAs per hash
+  const int hs = blockIdx.x / cps;
+  const int sg0 = (blockIdx.x % cps) * spc;
+  __shared__ double lnv[2], wu[2];
+  __shared__ uint32_t bits_s[kSegWords];
+  __shared__ int32_t warp_buf[kSampThreads / 32];
+  __shared__ int32_t next_s, prev_s;
+  __shared__ long long k0_s;
+  if (threadIdx.x < 2) {
+    const int h = hs / s, t = hs % s;
+    uint32_t c[4] = {(uint32_t)t, (uint32_t)h, 0u, 0u};
+    philox4x32_10(c, (uint32_t)(seed & 0xffffffffu), (uint32_t)(seed >> 32));
+    const double two_m32 = 0x1p-32;
+    const double uk = __dmul_rn(__dadd_rn((double)c[threadIdx.x], 0.5), two_m32);
+    lnv[threadIdx.x] = ln_rn(uk);
+    if (threadIdx.x == 0) wu[1] = __dmul_rn(__dadd_rn((double)c[2], 0.5), two_m32);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const double w = __dmul_rn(sigma[hs / s], __dadd_rn(-lnv[0], -lnv[1]));
+    const double u = __dmul_rn(w, wu[1]);
+    wu[0] = w;
+    wu[1] = u;
+    if (sg0 == 0) {
+      w_out[hs] = w;
+      u_out[hs] = u;
+    }
+  }
+  __syncthreads();
+  const double w = wu[0], u = wu[1];
+  for (int sg = sg0; sg < min(nseg, sg0 + spc); ++sg) {
+    const int64_t seg = (int64_t)sg * kSegWords;
+    const int nw = (int)min((int64_t)kSegWords, W - seg);
+    const int64_t P0 = seg * 32;
+    const int64_t P1 = min(P0 + (int64_t)nw * 32, n);
+    if (threadIdx.x < kSegWords) bits_s[threadIdx.x] = 0u;
+    if (threadIdx.x == 0) {
+      next_s = (int32_t)n;
+      prev_s = P0 > 0 ? 0 : -1;    // position 0 always opens a bin
+      // first k whose start can reach the segment: just below
+      // (P0 - 1 - u) / w, stepped back two to absorb rounding
+      const double est = w >= 1.0 ? floor(((double)(P0 - 1) - u) / w) - 2.0 : 0.0;
+      k0_s = est > 0.0 ? (long long)est : 0ll;
+    }
+    __syncthreads();
+    if (w < 1.0) {   // every position opens a bin
+      if (threadIdx.x < nw) {
+        const int64_t lo = P0 + (int64_t)threadIdx.x * 32;
+        const int64_t cnt = min((int64_t)32, P1 - lo);
+        bits_s[threadIdx.x] = cnt >= 32 ? 0xffffffffu : ((1u << cnt) - 1u);
+      }
+      if (threadIdx.x == 0) {
+        if (P0 > 0) prev_s = (int32_t)(P0 - 1);
+        if (P1 < n) next_s = (int32_t)P1;
+      }
+    } else {
+      if (P0 == 0 && threadIdx.x == 0) atomicOr(&bits_s[0], 1u);
+      // k from k0 while the exact start stays below P1; starts below P0 give
+      // the last start before the segment, the first at or past P1 the next
+      const long long k0 = k0_s;
+      int32_t before = -1;
+      for (long long k = k0 + threadIdx.x;; k += kSampThreads) {
+        const double c = start_of(k, w, u);
+        if (c >= (double)P1) {
+          if (c < (double)n) atomicMin(&next_s, (int32_t)c);
+          break;
+        }
+        if (c >= (double)P0) {
+          const int64_t off = (int64_t)c - P0;
+          atomicOr(&bits_s[off >> 5], 1u << (off & 31));
+        } else {
+          before = max(before, (int32_t)c);
+        }
+      }
+      if (before >= 0) atomicMax(&prev_s, before);
+    }
+    __syncthreads();
+    const uint32_t bits = threadIdx.x < nw ? bits_s[threadIdx.x] : 0u;
+    const int64_t wd = seg + threadIdx.x;
+    const int32_t hi_pos = bits ? (int32_t)(wd * 32 + 31 - __clz(bits)) : -1;
+    const int32_t lo_pos = bits ? (int32_t)(wd * 32 + __ffs(bits) - 1) : (int32_t)n;
+    const int32_t prev = max(block_excl_scan(hi_pos, true, -1, warp_buf), prev_s);
+    const int32_t next = min(block_excl_scan(lo_pos, false, (int32_t)n, warp_buf), next_s);
+    if (threadIdx.x < nw) {
+      BinRecord o;
+      o.bits = bits;
+      o.prev = (bits & 1u) ? (int32_t)(wd * 32) : prev;
+      o.next = next;
+      o.pad = 0;
+      rec[(int64_t)hs * W + wd] = o;
+    }
+    __syncthreads();
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_sample(plsh_bins* b, uint64_t seed, cudaStream_t st) {
   const int HS = b->H * b->s;
-  draw_kernel<<<(HS + 127) / 128, 128, 0, st>>>(b->d_sigma, b->H, b->s, seed,
-                                                 b->d_w, b->d_u);
-  const int64_t total = (int64_t)HS * b->W;
-  bits_from_draws_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(
-      b->n, b->W, HS, b->d_w, b->d_u, b->d_rec);
-  prev_next_kernel<<<HS, kScanThreads, 0, st>>>(b->n, b->W, b->d_rec);
+  // about 2048 CTAs whatever the shape: each takes spc consecutive segments
+  // of one hash and computes that hash's draw once
+  const int64_t nseg = (b->W + kSegWords - 1) / kSegWords;
+  const int64_t target = 2048;
+  const int64_t spc = std::max<int64_t>(1, (HS * nseg + target - 1) / target);
+  const int64_t cps = (nseg + spc - 1) / spc;
+  sample_kernel<<<(unsigned)(HS * cps), kSampThreads, 0, st>>>(
+      b->n, b->W, (int)nseg, (int)spc, b->s, b->d_sigma, seed, b->d_w, b->d_u, b->d_rec);
   return cudaGetLastError();
 }
 

@@ -100,6 +100,7 @@ SMALL = [
     ("bf16_causal_ragged", 1, 4, 2, 1000, 128, "bf16", True, 10, (1.2, 6.0, 40.0, 300.0)),
     ("bf16_noncausal_ragged", 2, 2, 1, 777, 128, "bf16", False, 6, (3.0, 150.0)),
     ("bf16_d64", 1, 2, 1, 513, 64, "bf16", True, 4, (5.0, 60.0)),
+    ("bf16_s24", 1, 2, 1, 700, 128, "bf16", True, 24, (3.0, 50.0)),
     ("bf16_s48", 1, 2, 2, 640, 128, "bf16", True, 48, (2.0, 30.0)),
     ("bf16_s64", 1, 2, 2, 640, 128, "bf16", True, 64, (2.0, 30.0)),
     ("bf16_noncausal_s30", 1, 2, 1, 400, 128, "bf16", False, 30, (0.8, 40.0)),
