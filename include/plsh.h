@@ -151,6 +151,37 @@ plsh_status plsh_alibi_attn(const plsh_tensor* Q, const plsh_tensor* K,
                             int32_t causal, plsh_tensor* O, void* stream);
 
 /*
+ * plsh_alibi_attn_noalloc -- plsh_alibi_attn for callers that may not
+ * allocate device memory.  The paper has no counterpart: this is a
+ * deployment variant, not part of the method.
+ *
+ * Some callers cannot let a library call cudaMalloc: a serving process that
+ * has reserved all of HBM for its own pools (a late allocation would fail or
+ * fragment it), or a latency-bound loop where an allocation's implicit
+ * device synchronisation is not acceptable.  This entry point computes the
+ * same result as plsh_alibi_attn with the same arguments and rules, but keeps
+ * its working memory (the work-item table and the work-queue counters) in a
+ * fixed array compiled into the library, about 1 MiB per device, held by
+ * every device that loads the library until the process exits.  It calls no
+ * allocation routine.
+ *
+ * Limits: bf16, d = 128, s within the tensor-core kernel's shared-memory
+ * budget (s <= 40 causal), at most 1023 query heads and 65536 work items
+ * (one item per two 128-row query tiles: B * Hq * ceil(n/128) / 2, e.g.
+ * n = 131072 with 40 heads uses 20480); larger requests return
+ * PLSH_ERR_UNSUPPORTED and launch nothing.
+ * The first call on each device resolves the array's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * Every call on a device shares the one array and each call resets it before
+ * use, so calls whose kernels overlap on the GPU (different streams without
+ * ordering) race and must not be issued.  Device-side wait timeouts of this
+ * path are recorded in the array, not reported by plsh_stream_status().
+ */
+plsh_status plsh_alibi_attn_noalloc(const plsh_tensor* Q, const plsh_tensor* K,
+                                    const plsh_tensor* V, const plsh_bins* bins,
+                                    int32_t causal, plsh_tensor* O, void* stream);
+
+/*
  * plsh_alibi_exact -- exact ALiBi attention T* (the dense comparator, Problem
  * statement: O(n^2) in the bias matrix):
  *   O_i = sum_j e^{S_ij - |i-j|/sigma_h} v_j / sum_j e^{S_ij - |i-j|/sigma_h}

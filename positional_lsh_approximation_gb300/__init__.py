@@ -21,6 +21,7 @@ import torch
 from . import build as _build_mod
 
 __all__ = ["build", "load", "sample_bins", "bins_from_host", "Bins", "alibi_attn",
+           "alibi_attn_noalloc",
            "alibi_exact", "stream_status", "set_wait_limit_ns", "PlshError",
            "library_path"]
 
@@ -78,6 +79,7 @@ def load():
             "plsh_bins_to_host": [P, ctypes.POINTER(I64), ctypes.POINTER(I32), I64, P],
             "plsh_bins_draws": [P, D, D, P],
             "plsh_alibi_attn": [TP, TP, TP, P, I32, TP, P],
+            "plsh_alibi_attn_noalloc": [TP, TP, TP, P, I32, TP, P],
             "plsh_alibi_exact": [TP, TP, TP, D, I32, TP, P],
             "plsh_stream_status": [P],
             "plsh_set_wait_limit_ns": [U64],
@@ -234,6 +236,12 @@ def _run(fn, Q, K, V, extra, causal, out, stream):
 def alibi_attn(Q, K, V, bins: Bins, causal: bool, out=None, stream=None):
     """plsh_alibi_attn: approximate ALiBi attention T~ (Methodology 3)."""
     return _run(load().plsh_alibi_attn, Q, K, V, bins.handle, causal, out, stream)
+
+
+def alibi_attn_noalloc(Q, K, V, bins: Bins, causal: bool, out=None, stream=None):
+    """plsh_alibi_attn_noalloc: plsh_alibi_attn without any device allocation
+    inside the call (fixed scratch compiled into the library)."""
+    return _run(load().plsh_alibi_attn_noalloc, Q, K, V, bins.handle, causal, out, stream)
 
 
 def alibi_exact(Q, K, V, sigma, causal: bool, out=None, stream=None):

@@ -373,6 +373,53 @@ plsh_status run_attention(const plsh_tensor* Q, const plsh_tensor* K, const plsh
 
 }  // namespace
 
+// ------------------------------------------------------- allocation-free path
+// plsh_alibi_attn_noalloc keeps its scratch (work-queue counters and the
+// work-item table of the tensor-core kernel) in this fixed device array
+// instead of library-allocated memory.  Element 0 holds {next item, finished
+// CTAs, device error flag, unused}; elements 1.. hold the items.  Every call
+// on a device uses the same array.
+constexpr int kNoAllocMaxItems = 65536;
+static __device__ __align__(256) int4 g_noalloc_scratch[1 + kNoAllocMaxItems];
+
+// Device address of g_noalloc_scratch per device, resolved once per device.
+int4* g_noalloc_addr[kMaxDevices] = {};
+std::mutex g_noalloc_mu;
+
+constexpr int kNoAllocMaxUnits = 512;
+
+// Work units in cost order: a pair of heads of one KV group (every row tile
+// is an item), or the last head of an odd group (pairs of its row tiles).
+struct NoAllocUnits {
+  int count;
+  int unit[kNoAllocMaxUnits];   // hA | hB << 10 | leftover << 20
+};
+
+// One thread per work item: writes the item table the tensor-core kernel
+// reads, in unit order, batch-major inside a unit; thread 0 also clears the
+// queue counters and the error flag.
+__global__ void noalloc_items_kernel(int4* scratch, const __grid_constant__ NoAllocUnits u,
+                                     int B, int QT, int num_items) {
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx == 0) scratch[0] = make_int4(0, 0, 0, 0);
+  if (idx >= num_items) return;
+  int off = idx;
+  for (int k = 0; k < u.count; ++k) {
+    const int code = u.unit[k];
+    const bool leftover = (code >> 20) & 1;
+    const int per_b = leftover ? (QT + 1) / 2 : QT;
+    if (off < B * per_b) {
+      const int b = off / per_b, q = off % per_b;
+      const int hA = code & 1023, hB = (code >> 10) & 1023;
+      const int qtA = leftover ? 2 * q : q;
+      const int qtB = leftover ? (2 * q + 1 < QT ? 2 * q + 1 : -1) : q;
+      scratch[1 + idx] = make_int4(b, hA | (hB << 16), qtA, qtB);
+      return;
+    }
+    off -= B * per_b;
+  }
+}
+
 extern "C" {
 
 plsh_status plsh_sample_bins(int64_t n, const double* sigma_h, int32_t H, int32_t s,
@@ -568,5 +615,118 @@ const char* plsh_status_string(plsh_status status) {
 }
 
 const char* plsh_last_error(void) { return g_last_error.c_str(); }
+
+// Allocation-free variant of plsh_alibi_attn (see include/plsh.h).
+plsh_status plsh_alibi_attn_noalloc(const plsh_tensor* Q, const plsh_tensor* K,
+                                    const plsh_tensor* V, const plsh_bins* bins,
+                                    int32_t causal, plsh_tensor* O, void* stream) {
+  plsh_status st = check_qkvo(Q, K, V, O);
+  if (st != PLSH_OK) return st;
+  if (bins == nullptr) return fail(PLSH_ERR_INVALID, "bins is NULL");
+  if (bins->n != Q->n) return fail(PLSH_ERR_INVALID, "bins were drawn for another n");
+  if (bins->H != Q->H) return fail(PLSH_ERR_INVALID, "bins were drawn for another number of heads");
+  if ((st = check_bins_device(bins)) != PLSH_OK) return st;
+  if (Q->dtype != PLSH_BF16 || Q->d != 128 ||
+      plsh::attn_tc_smem_bytes(bins->s, causal ? 1 : 0, 0) > 232448)
+    return fail(PLSH_ERR_UNSUPPORTED, "allocation-free path: needs bf16, d = 128 and s within "
+                                      "the tensor-core kernel's shared-memory budget");
+  const int B = (int)Q->B, Hq = (int)Q->H, Hkv = (int)K->H;
+  const int QT = (int)((Q->n + 127) / 128);
+  const int G = Hq / Hkv;
+  if (Hq > 1023 || Hkv * (G / 2 + G % 2) > kNoAllocMaxUnits)
+    return fail(PLSH_ERR_UNSUPPORTED, "allocation-free path: at most 1023 query heads and " +
+                                          std::to_string(kNoAllocMaxUnits) + " work units");
+  // units in cost order, built on the stack
+  NoAllocUnits u;
+  u.count = 0;
+  double key[kNoAllocMaxUnits];
+  int64_t num_items = 0;
+  for (int kvh = 0; kvh < Hkv; ++kvh) {
+    int heads[1024];
+    for (int gi = 0; gi < G; ++gi) heads[gi] = kvh * G + gi;
+    for (int a = 1; a < G; ++a) {          // by sigma, descending (stable)
+      const int h = heads[a];
+      int b2 = a;
+      while (b2 > 0 && bins->sigma_host[heads[b2 - 1]] < bins->sigma_host[h]) {
+        heads[b2] = heads[b2 - 1];
+        --b2;
+      }
+      heads[b2] = h;
+    }
+    for (int pr = 0; pr + 1 < G; pr += 2) {
+      u.unit[u.count] = heads[pr] | (heads[pr + 1] << 10);
+      key[u.count] = std::max(bins->sigma_host[heads[pr]], bins->sigma_host[heads[pr + 1]]);
+      ++u.count;
+      num_items += (int64_t)B * QT;
+    }
+    if (G % 2) {
+      u.unit[u.count] = heads[G - 1] | (heads[G - 1] << 10) | (1 << 20);
+      key[u.count] = bins->sigma_host[heads[G - 1]];
+      ++u.count;
+      num_items += (int64_t)B * ((QT + 1) / 2);
+    }
+  }
+  for (int a = 1; a < u.count; ++a) {      // units by cost, descending (stable)
+    const int cu = u.unit[a];
+    const double ck = key[a];
+    int b2 = a;
+    while (b2 > 0 && key[b2 - 1] < ck) {
+      u.unit[b2] = u.unit[b2 - 1];
+      key[b2] = key[b2 - 1];
+      --b2;
+    }
+    u.unit[b2] = cu;
+    key[b2] = ck;
+  }
+  if (num_items > kNoAllocMaxItems)
+    return fail(PLSH_ERR_UNSUPPORTED,
+                "allocation-free path: " + std::to_string(num_items) + " work items exceed its " +
+                    std::to_string(kNoAllocMaxItems) + "-item scratch area");
+  int dev = -1;
+  PLSH_TRY_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(PLSH_ERR_UNSUPPORTED, "device index out of range");
+  int4* scratch = nullptr;
+  {
+    // set-up, once per device with that device current: the array's host
+    // name is not a device address, so resolve it here
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (g_noalloc_addr[dev] == nullptr) {
+      void* ptr = nullptr;
+      PLSH_TRY_CUDA(cudaGetSymbolAddress(&ptr, g_noalloc_scratch), "cudaGetSymbolAddress");
+      g_noalloc_addr[dev] = static_cast<int4*>(ptr);
+    }
+    scratch = g_noalloc_addr[dev];
+  }
+  int sms = 0;
+  PLSH_TRY_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev),
+                "cudaDeviceGetAttribute");
+  cudaStream_t cs = (cudaStream_t)stream;
+  noalloc_items_kernel<<<(unsigned)((num_items + 255) / 256), 256, 0, cs>>>(
+      scratch, u, B, QT, (int)num_items);
+  PLSH_TRY_CUDA(cudaGetLastError(), "item table launch");
+  plsh::AttnArgs a;
+  memset(&a, 0, sizeof a);
+  a.Q = Q->data;
+  a.K = K->data;
+  a.V = V->data;
+  a.O = O->data;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.n = (int)Q->n;
+  a.d = (int)Q->d;
+  a.causal = causal ? 1 : 0;
+  a.exact = 0;
+  a.rec = bins->d_rec;
+  a.s = bins->s;
+  a.W = bins->W;
+  a.items = scratch + 1;
+  a.num_items = (int)num_items;
+  a.queue = reinterpret_cast<int*>(scratch);
+  a.err = reinterpret_cast<int*>(scratch) + 2;
+  a.wait_ns = plsh::kDefaultWaitNs;
+  PLSH_TRY_CUDA(plsh::launch_attn_tc(a, nullptr, sms, cs), "attention launch");
+  return PLSH_OK;
+}
 
 }  // extern "C"
