@@ -712,32 +712,43 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
           } else if (SREG > 0) {
             vm = key_mask(vlo - jc, vhi - jc, row_ok);
             // rows past every bin start of the chunk (and before every end)
-            // have c = s throughout; otherwise count the registers
+            // have c = s throughout; otherwise one pass over the registers
+            // counts the starts at or before jc and marks the steps inside
             const bool deep = lomax <= jc && (CAUSAL || himin > jc + 31);
             if (__all_sync(FULL, deep || vm == 0u)) {
               base = s;
             } else {
-              bool any = false;
+              uint32_t dup = 0u;
 #pragma unroll
               for (int t = 0; t < (SREG > 0 ? SREG : 1); ++t) {
                 const int dl = lo_r[t] - jc;
                 base += dl <= 0 ? 1 : 0;
-                any = any || (unsigned)(dl - 1) < 31u;
+                const uint32_t bit = (unsigned)(dl - 1) < 31u ? (1u << dl) : 0u;
+                dup |= up[0] & bit;
+                up[0] |= bit;
                 if (!CAUSAL) {
                   const int dh = hi_r[t] - jc;
                   base -= dh <= 0 ? 1 : 0;
-                  any = any || (unsigned)(dh - 1) < 31u;
+                  const uint32_t bh = (unsigned)(dh - 1) < 31u ? (1u << dh) : 0u;
+                  dup |= dn[0] & bh;
+                  dn[0] |= bh;
                 }
               }
-              flat = !any || vm == 0u;
-              if (__any_sync(FULL, !flat)) {
+              if (vm == 0u) { up[0] = 0u; dn[0] = 0u; dup = 0u; }
+              flat = (up[0] | dn[0]) == 0u;
+              if (__any_sync(FULL, dup != 0u)) {
+                // several starts share a key: binary planes of multiplicities
+                up[0] = 0u;
+                dn[0] = 0u;
+                if (vm != 0u) {
 #pragma unroll
-                for (int t = 0; t < (SREG > 0 ? SREG : 1); ++t) {
-                  const int dl = lo_r[t] - jc;
-                  plane_add(up, (unsigned)(dl - 1) < 31u ? (1u << dl) : 0u);
-                  if (!CAUSAL) {
-                    const int dh = hi_r[t] - jc;
-                    plane_add(dn, (unsigned)(dh - 1) < 31u ? (1u << dh) : 0u);
+                  for (int t = 0; t < (SREG > 0 ? SREG : 1); ++t) {
+                    const int dl = lo_r[t] - jc;
+                    plane_add(up, (unsigned)(dl - 1) < 31u ? (1u << dl) : 0u);
+                    if (!CAUSAL) {
+                      const int dh = hi_r[t] - jc;
+                      plane_add(dn, (unsigned)(dh - 1) < 31u ? (1u << dh) : 0u);
+                    }
                   }
                 }
               }
