@@ -71,21 +71,21 @@ constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kSchedWarp = 10;
 constexpr int kRing = 3;                         // work items in flight
-constexpr int kSlots = 3;                        // K/V tile ring
+constexpr int kMaxSlots = 4;                     // K/V tile ring (3 or 4 slots)
 constexpr uint32_t kTileBytes = BM * HD * 2;     // 32 KB bf16 tile
 constexpr uint32_t kHalfBytes = kTileBytes / 2;  // one 64-column TMA box
 constexpr uint32_t OFF_Q = 0;                          // Q_A, Q_B
-constexpr uint32_t OFF_KV = OFF_Q + 2 * kTileBytes;    // ring of kSlots
-constexpr uint32_t OFF_BP = OFF_KV + kSlots * kTileBytes;
+constexpr uint32_t OFF_KV = OFF_Q + 2 * kTileBytes;    // ring of `slots` tiles
 constexpr uint32_t kTmemCols = 512;   // S_A | S_B | O_A | O_B; P over S
 constexpr uint32_t kColO = 256;
 constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (factor 256)
 constexpr unsigned FULL = 0xffffffffu;
 constexpr int kWordsPerTile = BM / 32;
+constexpr uint32_t kOutBytes = 8 * 32 * 64 * 2;   // O transpose: 32 rows x 64 bf16 per warp
 
 enum {
-  B_QFULL = 0, B_QFULL1, B_QEMPTY, B_QEMPTY1, B_KVFULL, B_KVFULL_END = B_KVFULL + kSlots,
-  B_KVEMPTY = B_KVFULL_END, B_KVEMPTY_END = B_KVEMPTY + kSlots,
+  B_QFULL = 0, B_QFULL1, B_QEMPTY, B_QEMPTY1, B_KVFULL, B_KVFULL_END = B_KVFULL + kMaxSlots,
+  B_KVEMPTY = B_KVFULL_END, B_KVEMPTY_END = B_KVEMPTY + kMaxSlots,
   B_SFULL = B_KVEMPTY_END, B_SFULL1, B_PFULL, B_PFULL1, B_ODONE, B_ODONE1,
   B_IFULL, B_IFULL_END = B_IFULL + kRing, B_IEMPTY = B_IFULL_END,
   B_IEMPTY_END = B_IEMPTY + kRing, B_DRAIN = B_IEMPTY_END, NUM_BARS
@@ -106,6 +106,8 @@ struct TcParams {
   AttnArgs a;
   float slope_log2[512];   // exact mode: log2(e) / sigma_h
   int QT;                  // query tiles per (b, h)
+  int slots;               // K/V ring depth
+  int out_smem;            // 1: the epilogue transposes O through shared memory
 };
 
 // Sorted bin starts (and ends when not causal) of every row of both tiles:
@@ -144,10 +146,6 @@ __device__ __forceinline__ uint32_t key_mask(int ea, int eb, bool row_ok) {
   return up & dn;
 }
 
-// Multiplies the chunk's weights by the running step count c(e): base plus
-// the binary planes of step multiplicities at each key (up) minus those of
-// bin ends (dn, non-causal only), L planes in use.
-
 // Adds one step at the positions of `m` to a five-plane binary counter.
 __device__ __forceinline__ void plane_add(uint32_t (&pl)[5], uint32_t m) {
 #pragma unroll
@@ -157,26 +155,74 @@ __device__ __forceinline__ void plane_add(uint32_t (&pl)[5], uint32_t m) {
     m = c;
   }
 }
+
+// Multiplies the chunk's weights by the running count c(e): base plus the
+// binary planes of step multiplicities at each key (up) minus those of bin
+// ends (dn, non-causal only), L planes in use; four independent runs of
+// eight keys.
 template <int L, bool CAUSAL>
-__device__ __forceinline__ void scale_by_count(float (&pv)[32], float base,
-                                               const uint32_t (&up)[5],
-                                               const uint32_t (&dn)[5]) {
-  float cf = base;
+__device__ __forceinline__ void scale_by_planes(float (&pv)[32], int base,
+                                                const uint32_t (&up)[5],
+                                                const uint32_t (&dn)[5]) {
+  float c[4];
 #pragma unroll
-  for (int e2 = 0; e2 < 16; ++e2) {
-    float c2[2];
+  for (int g = 0; g < 4; ++g) {
+    const uint32_t below = (1u << (8 * g)) - 1u;
+    int cb = base;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint32_t bit = 1u << (2 * e2 + h);
-#pragma unroll
-      for (int b = 0; b < L; ++b) {
-        if (up[b] & bit) cf += (float)(1 << b);
-        if (!CAUSAL && (dn[b] & bit)) cf -= (float)(1 << b);
-      }
-      c2[h] = cf;
+    for (int b = 0; b < L; ++b) {
+      cb += __popc(up[b] & below) << b;
+      if (!CAUSAL) cb -= __popc(dn[b] & below) << b;
     }
-    const uint64_t p2 = f2_mul(f2_pack(pv[2 * e2], pv[2 * e2 + 1]), f2_pack(c2[0], c2[1]));
-    f2_unpack(p2, pv[2 * e2], pv[2 * e2 + 1]);
+    c[g] = (float)cb;
+  }
+#pragma unroll
+  for (int k = 0; k < 8; k += 2) {
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const int e = 8 * g + k;
+      float ce = 0.f;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+#pragma unroll
+        for (int b = 0; b < L; ++b) {
+          if (up[b] & (1u << (e + h))) c[g] += (float)(1 << b);
+          if (!CAUSAL && (dn[b] & (1u << (e + h)))) c[g] -= (float)(1 << b);
+        }
+        if (h == 0) ce = c[g];
+      }
+      const uint64_t p2 = f2_mul(f2_pack(pv[e], pv[e + 1]), f2_pack(ce, c[g]));
+      f2_unpack(p2, pv[e], pv[e + 1]);
+    }
+  }
+}
+
+// The same for chunks where no two starts (or ends) share a key: one bit
+// per step, counted in four independent runs of eight keys.
+template <bool CAUSAL>
+__device__ __forceinline__ void scale_by_steps(float (&pv)[32], int base,
+                                               uint32_t up, uint32_t dn) {
+  float c[4];
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    const uint32_t below = (1u << (8 * g)) - 1u;
+    int cb = base + __popc(up & below);
+    if (!CAUSAL) cb -= __popc(dn & below);
+    c[g] = (float)cb;
+  }
+#pragma unroll
+  for (int k = 0; k < 8; k += 2) {
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const int e = 8 * g + k;
+      if (up & (1u << e)) c[g] += 1.f;
+      if (!CAUSAL && (dn & (1u << e))) c[g] -= 1.f;
+      const float ce = c[g];
+      if (up & (2u << e)) c[g] += 1.f;
+      if (!CAUSAL && (dn & (2u << e))) c[g] -= 1.f;
+      const uint64_t p2 = f2_mul(f2_pack(pv[e], pv[e + 1]), f2_pack(ce, c[g]));
+      f2_unpack(p2, pv[e], pv[e + 1]);
+    }
   }
 }
 
@@ -196,9 +242,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
   const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (sbase - raw_u32);
   const int s = a.s;
-  int* bp = reinterpret_cast<int*>(smem + OFF_BP);
-  uint4* stage = reinterpret_cast<uint4*>(smem + OFF_BP + bp_bytes(s, EXACT, CAUSAL, SREG));
-  Ctl* ctl = reinterpret_cast<Ctl*>(smem + OFF_BP + bp_bytes(s, EXACT, CAUSAL, SREG) +
+  const int nslots = p.slots;
+  const uint32_t off_out = OFF_KV + (uint32_t)nslots * kTileBytes;   // 8 warps x 4 KB
+  const uint32_t off_bp = off_out + (p.out_smem ? kOutBytes : 0u);
+  int* bp = reinterpret_cast<int*>(smem + off_bp);
+  uint4* stage = reinterpret_cast<uint4*>(smem + off_bp + bp_bytes(s, EXACT, CAUSAL, SREG));
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + off_bp + bp_bytes(s, EXACT, CAUSAL, SREG) +
                                     stage_bytes(s, EXACT));
   auto bar = [&](int k) { return smem_u32(&ctl->bars[k]); };
   volatile int* abort = &ctl->abort;
@@ -209,7 +258,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       mbar_init(bar(B_QFULL + k), 1);
       mbar_init(bar(B_QEMPTY + k), 1);
     }
-    for (int k = 0; k < kSlots; ++k) {
+    for (int k = 0; k < kMaxSlots; ++k) {
       mbar_init(bar(B_KVFULL + k), 1);
       mbar_init(bar(B_KVEMPTY + k), 1);
     }
@@ -345,7 +394,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
     if (lane == 0) {
       int ld = 0;                       // K/V loads issued (K and V alternate)
       int q_issued = 0;
-      int kv_issued[kSlots] = {0, 0, 0};
+      int kv_issued[kMaxSlots] = {0, 0, 0, 0};
       bool ok = true;
       for (int seq = 0; ok; ++seq) {
         const int slot = seq % kRing;
@@ -354,24 +403,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         if (!ok) break;
         const Item it = read_item(ctl, slot);
         if (!it.valid) break;
-        for (int tile = 0; tile < 2 && ok; ++tile) {
-          ok = mbar_wait(bar(B_QEMPTY + tile), ((uint32_t)seq & 1u) ^ 1u, abort, lim);
-          if (!ok) break;
-          // an unused tile B reloads A's rows so its scores stay finite
-          const int qt = (tile && it.qtB >= 0) ? it.qtB : it.qtA;
-          const int h = (tile && it.qtB >= 0) ? it.hB : it.hA;
-          const uint32_t qdst = sbase + OFF_Q + tile * kTileBytes;
-          mbar_arrive_expect_tx(bar(B_QFULL + tile), kTileBytes);
-          tma_load_3d(qdst, &tmQ, bar(B_QFULL + tile), 0, qt * BM, it.b * Hq + h);
-          tma_load_3d(qdst + kHalfBytes, &tmQ, bar(B_QFULL + tile), 64, qt * BM, it.b * Hq + h);
-        }
-        if (!ok) break;
-        ++q_issued;
+        // the item's first K tile goes first: it does not wait for the Q
+        // buffers, which free only when the item before has issued its last S
         const int kvp = it.b * Hkv + it.hA / (Hq / Hkv);
         for (int kt = it.kt_hi - 1; ok && kt >= it.kt_lo; --kt) {
           for (int kv = 0; kv < 2 && ok; ++kv, ++ld) {
-            const int sl = ld % kSlots;
-            const uint32_t u = (uint32_t)(ld / kSlots);
+            const int sl = ld % nslots;
+            const uint32_t u = (uint32_t)(ld / nslots);
             ok = mbar_wait(bar(B_KVEMPTY + sl), (u & 1u) ^ 1u, abort, lim);
             if (!ok) break;
             const uint32_t dst = sbase + OFF_KV + sl * kTileBytes;
@@ -380,6 +418,21 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
             tma_load_3d(dst, m, bar(B_KVFULL + sl), 0, kt * BN, kvp);
             tma_load_3d(dst + kHalfBytes, m, bar(B_KVFULL + sl), 64, kt * BN, kvp);
             ++kv_issued[sl];
+            if (kt == it.kt_hi - 1 && kv == 0) {
+              for (int tile = 0; tile < 2 && ok; ++tile) {
+                ok = mbar_wait(bar(B_QEMPTY + tile), ((uint32_t)seq & 1u) ^ 1u, abort, lim);
+                if (!ok) break;
+                // an unused tile B reloads A's rows so its scores stay finite
+                const int qt = (tile && it.qtB >= 0) ? it.qtB : it.qtA;
+                const int h = (tile && it.qtB >= 0) ? it.hB : it.hA;
+                const uint32_t qdst = sbase + OFF_Q + tile * kTileBytes;
+                mbar_arrive_expect_tx(bar(B_QFULL + tile), kTileBytes);
+                tma_load_3d(qdst, &tmQ, bar(B_QFULL + tile), 0, qt * BM, it.b * Hq + h);
+                tma_load_3d(qdst + kHalfBytes, &tmQ, bar(B_QFULL + tile), 64, qt * BM,
+                            it.b * Hq + h);
+              }
+              if (ok) ++q_issued;
+            }
           }
         }
         if (ok) mbar_arrive(bar(B_IEMPTY + slot));
@@ -393,7 +446,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         mbar_wait(bar(B_QFULL + 0), (uint32_t)(q_issued - 1) & 1u, nullptr, lim);
         mbar_wait(bar(B_QFULL + 1), (uint32_t)(q_issued - 1) & 1u, nullptr, lim);
       }
-      for (int sl = 0; sl < kSlots; ++sl)
+      for (int sl = 0; sl < nslots; ++sl)
         if (kv_issued[sl])
           mbar_wait(bar(B_KVFULL + sl), (uint32_t)(kv_issued[sl] - 1) & 1u, nullptr, lim);
     }
@@ -407,11 +460,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       int ld = 0;        // K/V loads consumed so far (same numbering as producer)
       int gt = 0;        // tiles processed so far (both tiles advance together)
       auto wait_slot = [&](int l) -> bool {
-        return mbar_wait(bar(B_KVFULL + l % kSlots), (uint32_t)(l / kSlots) & 1u, abort, lim);
+        return mbar_wait(bar(B_KVFULL + l % nslots), (uint32_t)(l / nslots) & 1u, abort, lim);
       };
       auto issue_s = [&](int tile, int lk) {
         const uint32_t qbase = sbase + OFF_Q + tile * kTileBytes;
-        const uint32_t kbase = sbase + OFF_KV + (lk % kSlots) * kTileBytes;
+        const uint32_t kbase = sbase + OFF_KV + (lk % nslots) * kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t koff = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
@@ -421,7 +474,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         mma_commit(bar(B_SFULL + tile));
       };
       auto issue_pv = [&](int tile, int lv, bool first) {
-        const uint32_t vbase = sbase + OFF_KV + (lv % kSlots) * kTileBytes;
+        const uint32_t vbase = sbase + OFF_KV + (lv % nslots) * kTileBytes;
         // keys 16kk..16kk+15 sit in chunk kk/2: P_hi in its first 16
         // columns, P_lo in the next 16, 8 packed columns per 16 keys
         const uint32_t pcol = tmem + tile * BN;
@@ -468,7 +521,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
           if (!ok) break;
           tc_fence_after();
           issue_pv(1, prev_lv, prev_first);
-          mma_commit(bar(B_KVEMPTY + prev_lv % kSlots));
+          mma_commit(bar(B_KVEMPTY + prev_lv % nslots));
           if (prev_last) {
             mma_commit(bar(B_ODONE + 1));
             mbar_arrive(bar(B_IEMPTY + prev_slot));
@@ -480,7 +533,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         }
         tc_fence_after();
         issue_s(1, lk);
-        mma_commit(bar(B_KVEMPTY + lk % kSlots));
+        mma_commit(bar(B_KVEMPTY + lk % nslots));
         if (jj == T - 1) mma_commit(bar(B_QEMPTY + 1));
         have_prev = true;
         prev_lv = lk + 1;
@@ -511,7 +564,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         if (ok) {
           tc_fence_after();
           issue_pv(1, prev_lv, prev_first);
-          mma_commit(bar(B_KVEMPTY + prev_lv % kSlots));
+          mma_commit(bar(B_KVEMPTY + prev_lv % nslots));
           mma_commit(bar(B_ODONE + 1));
           mbar_arrive(bar(B_IEMPTY + prev_slot));
         }
@@ -539,13 +592,86 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
     int* bph = bpl + s * BM;                     // sorted bin ends (non-causal)
     bool ok = true;
     int g = 0;
+    // with bin lists in shared memory the output of an item is written once
+    // the next item is set up (the sort hides the item's last P V); with
+    // starts in registers the set-up is short and the output goes first
+    constexpr bool kDefer = SREG == 0;
+    bool pend = false;
+    float pend_l = 0.f;
+    const uint32_t obuf = sbase + off_out + (uint32_t)warp * 4096u;
+    // epilogue of item pseq: O_i = acc_i / l_i, then its item slot is released
+    auto finish = [&](int pseq) -> bool {
+      if (!__all_sync(FULL, mbar_wait(bar(B_ODONE + tile), (uint32_t)pseq & 1u, abort, lim)))
+        return false;
+      tc_fence_after();
+      // the item stays in its ring slot until this thread releases it
+      const int pslot = pseq % kRing;
+      const Item pit = read_item(ctl, pslot);
+      const int qt = tile ? pit.qtB : pit.qtA;
+      const int h = tile ? pit.hB : pit.hA;
+      const int i = max(qt, 0) * BM + r;
+      const int64_t row0 = ((int64_t)pit.b * Hq + h) * n;
+      const float inv_l = pend_l > 0.f ? 1.f / pend_l : 0.f;
+#pragma unroll 1
+      for (int q2 = 0; q2 < 2; ++q2) {
+        uint32_t o0[32], o1[32];
+        tmem_ld32(o_col + q2 * 64, o0);
+        tmem_ld32(o_col + q2 * 64 + 32, o1);
+        tmem_wait_ld();
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const uint32_t* o = half ? o1 : o0;
+          uint32_t pk[16];
+#pragma unroll
+          for (int e2 = 0; e2 < 16; ++e2)
+            pk[e2] = pack_bf16(__uint_as_float(o[2 * e2]) * inv_l,
+                               __uint_as_float(o[2 * e2 + 1]) * inv_l);
+          if (p.out_smem) {
+            // row-major 32 rows x 128 bytes, 16-byte chunks swizzled by row
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              st_shared_v4(obuf + lane * 128 + (((half * 4 + v) ^ (lane & 7)) << 4),
+                           pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          } else if (qt >= 0 && i < n) {
+            uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.O) +
+                                                   (row0 + i) * HD + q2 * 64);
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              orow[half * 4 + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          }
+        }
+        if (p.out_smem) {
+          // read back transposed: eight lanes write one row's 128 bytes, so
+          // every store instruction fills four whole lines
+          __syncwarp();
+          const int c = lane & 7;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int rr = 4 * k + (lane >> 3);
+            const uint4 v = ld_shared_v4(obuf + rr * 128 + ((c ^ (rr & 7)) << 4));
+            const int ir = max(qt, 0) * BM + (warp & 3) * 32 + rr;
+            if (qt >= 0 && ir < n)
+              reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.O) + (row0 + ir) * HD +
+                                       q2 * 64)[c] = v;
+          }
+          __syncwarp();
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar(B_IEMPTY + pslot));
+      pend = false;
+      return true;
+    };
     for (int seq = 0; ok; ++seq) {
       const int slot = seq % kRing;
       const uint32_t use = (uint32_t)(seq / kRing);
       ok = __all_sync(FULL, mbar_wait(bar(B_IFULL + slot), use & 1u, abort, lim));
       if (!ok) break;
       const Item it = read_item(ctl, slot);
-      if (!it.valid) break;
+      if (!it.valid) {
+        if (pend) ok = finish(seq - 1);
+        break;
+      }
       const int qt = tile ? it.qtB : it.qtA;
       const int h = tile ? it.hB : it.hA;
       const int i0 = max(qt, 0) * BM;
@@ -618,6 +744,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
 #pragma unroll
       for (int e2 = 0; e2 < 16; ++e2)
         eslope[e2] = f2_pack((float)(2 * e2) * slope, (float)(2 * e2 + 1) * slope);
+      if (pend) {
+        ok = finish(seq - 1);
+        if (!ok) break;
+      }
       float m_ref = -INFINITY, l = 0.f;
       for (int jj = 0; jj < ntiles; ++jj, ++g) {
         const int jt = (it.kt_hi - 1 - jj) * BN;
@@ -629,16 +759,31 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
         for (int q2 = 0; q2 < 2; ++q2) {
+          uint32_t vmh[2];
           uint32_t ra[32], rb2[32];
-          tmem_ld32(s_col + q2 * 64, ra);
-          tmem_ld32(s_col + q2 * 64 + 32, rb2);
+          if (EXACT) {
+            tmem_ld32(s_col + q2 * 64, ra);
+            tmem_ld32(s_col + q2 * 64 + 32, rb2);
+          }
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const int jc = jt + q2 * 64 + half * 32;
+            vmh[half] = EXACT ? key_mask(-1, CAUSAL ? i - jc : n - 1 - jc, row_ok)
+                              : key_mask(vlo - jc, vhi - jc, row_ok);
+          }
+          if (!EXACT) {
+            // 64 keys that no row of this warp takes: nothing to read
+            if (!__any_sync(FULL, (vmh[0] | vmh[1]) != 0u)) continue;
+            tmem_ld32(s_col + q2 * 64, ra);
+            tmem_ld32(s_col + q2 * 64 + 32, rb2);
+          }
           tmem_wait_ld();
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
             const uint32_t* rr = half ? rb2 : ra;
             const int jc = jt + q2 * 64 + half * 32;
             float xv[32];
-            uint32_t vm;
+            const uint32_t vm = vmh[half];
             if (EXACT) {
               const float d0 = (float)(i - jc);
 #pragma unroll
@@ -653,11 +798,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                                    -fabsf(d0 - (float)(e + 1)) * slope);
                 }
               }
-              vm = key_mask(-1, CAUSAL ? i - jc : n - 1 - jc, row_ok);
             } else {
 #pragma unroll
               for (int e = 0; e < 32; ++e) xv[e] = __uint_as_float(rr[e]);
-              vm = key_mask(vlo - jc, vhi - jc, row_ok);
             }
             if (__any_sync(FULL, vm != 0xffffffffu)) {
 #pragma unroll
@@ -702,59 +845,88 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         for (int q = 3; q >= 0; --q) {
           const int jc = jt + q * 32;
           uint32_t rr[32];
-          tmem_ld32(s_col + q * 32, rr);
-          int base = 0;
-          bool flat = true, big = false;
-          uint32_t up[5] = {0u, 0u, 0u, 0u, 0u}, dn[5] = {0u, 0u, 0u, 0u, 0u};
           uint32_t vm;
           if (EXACT) {
+            tmem_ld32(s_col + q * 32, rr);
             vm = key_mask(-1, CAUSAL ? i - jc : n - 1 - jc, row_ok);
-          } else if (SREG > 0) {
+          } else {
             vm = key_mask(vlo - jc, vhi - jc, row_ok);
+            if (!__any_sync(FULL, vm != 0u)) {
+              // no key of the chunk takes part in a row of this warp
+              const uint32_t z[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u,
+                                      0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+              tmem_st16(s_col + q * 32, z);
+              tmem_st16(s_col + q * 32 + 16, z);
+              continue;
+            }
+            tmem_ld32(s_col + q * 32, rr);
+          }
+          int base = 0;
+          bool flat = true, big = false, multi = true;
+          uint32_t up[5] = {0u, 0u, 0u, 0u, 0u}, dn[5] = {0u, 0u, 0u, 0u, 0u};
+          if (EXACT) {
+          } else if (SREG > 0) {
             // rows past every bin start of the chunk (and before every end)
-            // have c = s throughout; otherwise one pass over the registers
-            // counts the starts at or before jc and marks the steps inside
+            // have c = s throughout
             const bool deep = lomax <= jc && (CAUSAL || himin > jc + 31);
             if (__all_sync(FULL, deep || vm == 0u)) {
               base = s;
             } else {
-              uint32_t dup = 0u;
+              // starts at or before jc count into base, starts inside the
+              // chunk set their step bit; two accumulators for ILP (unused
+              // registers hold INT_MAX and add nothing)
+              const int jc1 = jc + 1;
+              int c0 = 0, c1 = 0;
+              uint32_t u0 = 0u, u1 = 0u, d0 = 0u, d1 = 0u, x0 = 0u, x1 = 0u;
 #pragma unroll
-              for (int t = 0; t < (SREG > 0 ? SREG : 1); ++t) {
-                const int dl = lo_r[t] - jc;
-                base += dl <= 0 ? 1 : 0;
-                const uint32_t bit = (unsigned)(dl - 1) < 31u ? (1u << dl) : 0u;
-                dup |= up[0] & bit;
-                up[0] |= bit;
+              for (int t = 0; t < (SREG > 0 ? SREG : 1); t += 2) {
+                if (t >= s) break;
+                {
+                  const int dm = lo_r[t] - jc1;
+                  c0 -= dm >> 31;
+                  const uint32_t bt = shl_clamp(2u, dm);
+                  x0 |= u0 & bt;
+                  u0 |= bt;
+                }
+                {
+                  const int dm = lo_r[t + 1] - jc1;
+                  c1 -= dm >> 31;
+                  const uint32_t bt = shl_clamp(2u, dm);
+                  x1 |= u1 & bt;
+                  u1 |= bt;
+                }
                 if (!CAUSAL) {
-                  const int dh = hi_r[t] - jc;
-                  base -= dh <= 0 ? 1 : 0;
-                  const uint32_t bh = (unsigned)(dh - 1) < 31u ? (1u << dh) : 0u;
-                  dup |= dn[0] & bh;
-                  dn[0] |= bh;
+                  const int da = hi_r[t] - jc1, db = hi_r[t + 1] - jc1;
+                  c0 += da >> 31;
+                  c1 += db >> 31;
+                  const uint32_t ba = shl_clamp(2u, da), bb = shl_clamp(2u, db);
+                  x0 |= d0 & ba;
+                  d0 |= ba;
+                  x1 |= d1 & bb;
+                  d1 |= bb;
                 }
               }
+              base = c0 + c1;
+              up[0] = u0 | u1;
+              dn[0] = d0 | d1;
+              uint32_t dup = x0 | x1 | (u0 & u1) | (d0 & d1);
               if (vm == 0u) { up[0] = 0u; dn[0] = 0u; dup = 0u; }
               flat = (up[0] | dn[0]) == 0u;
-              if (__any_sync(FULL, dup != 0u)) {
+              multi = __any_sync(FULL, dup != 0u);
+              if (multi) {
                 // several starts share a key: binary planes of multiplicities
                 up[0] = 0u;
                 dn[0] = 0u;
                 if (vm != 0u) {
 #pragma unroll
                   for (int t = 0; t < (SREG > 0 ? SREG : 1); ++t) {
-                    const int dl = lo_r[t] - jc;
-                    plane_add(up, (unsigned)(dl - 1) < 31u ? (1u << dl) : 0u);
-                    if (!CAUSAL) {
-                      const int dh = hi_r[t] - jc;
-                      plane_add(dn, (unsigned)(dh - 1) < 31u ? (1u << dh) : 0u);
-                    }
+                    plane_add(up, shl_clamp(2u, lo_r[t] - jc1));
+                    if (!CAUSAL) plane_add(dn, shl_clamp(2u, hi_r[t] - jc1));
                   }
                 }
               }
             }
           } else {
-            vm = key_mask(vlo - jc, vhi - jc, row_ok);
             while (pl > 0 && bpl[(pl - 1) * BM + r] > jc) --pl;
             while (ph > pl && bpl[(ph - 1) * BM + r] > jc + 31) --ph;
             base = pl;
@@ -798,10 +970,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
           }
           tmem_wait_ld();
           uint32_t hi[16], lo[16];
-          if (__all_sync(FULL, vm == 0u)) {
-#pragma unroll
-            for (int e2 = 0; e2 < 16; ++e2) { hi[e2] = 0u; lo[e2] = 0u; }
-          } else {
+          {
             const bool all_flat = EXACT || __all_sync(FULL, flat);
             float off;
             if (EXACT) off = -(float)(i - jc) * slope - mu;
@@ -835,7 +1004,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
               // c_ij inside the chunk: a running count of the bin starts
               // (minus bin ends), one plane per bit of the multiplicities
               const float fb = (float)base;
-              if (__any_sync(FULL, big)) {
+              if (SREG == 0 && __any_sync(FULL, big)) {
                 float cf[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) cf[e] = fb;
@@ -855,16 +1024,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                 }
 #pragma unroll
                 for (int e = 0; e < 32; ++e) pv[e] *= cf[e];
-              } else if (__any_sync(FULL, (up[4] | dn[4]) != 0u)) {
-                scale_by_count<5, CAUSAL>(pv, fb, up, dn);
-              } else if (__any_sync(FULL, (up[3] | dn[3]) != 0u)) {
-                scale_by_count<4, CAUSAL>(pv, fb, up, dn);
-              } else if (__any_sync(FULL, (up[2] | dn[2]) != 0u)) {
-                scale_by_count<3, CAUSAL>(pv, fb, up, dn);
-              } else if (__any_sync(FULL, (up[1] | dn[1]) != 0u)) {
-                scale_by_count<2, CAUSAL>(pv, fb, up, dn);
+              } else if (!multi) {
+                scale_by_steps<CAUSAL>(pv, base, up[0], dn[0]);
+              } else if (__any_sync(FULL, (up[2] | up[3] | up[4] | dn[2] | dn[3] | dn[4]) != 0u)) {
+                scale_by_planes<5, CAUSAL>(pv, base, up, dn);
               } else {
-                scale_by_count<1, CAUSAL>(pv, fb, up, dn);
+                scale_by_planes<2, CAUSAL>(pv, base, up, dn);
               }
             }
 #pragma unroll
@@ -892,37 +1057,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       }
       if (!ok) break;
 
-      // epilogue: O_i = acc_i / l_i
-      ok = __all_sync(FULL, mbar_wait(bar(B_ODONE + tile), (uint32_t)seq & 1u, abort, lim));
-      if (!ok) break;
-      tc_fence_after();
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
-      uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.O) +
-                                             (((int64_t)it.b * Hq + h) * n + ii) * HD);
-#pragma unroll
-      for (int q2 = 0; q2 < 2; ++q2) {
-        uint32_t o0[32], o1[32];
-        tmem_ld32(o_col + q2 * 64, o0);
-        tmem_ld32(o_col + q2 * 64 + 32, o1);
-        tmem_wait_ld();
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const uint32_t* o = half ? o1 : o0;
-          uint32_t pk[16];
-#pragma unroll
-          for (int e2 = 0; e2 < 16; ++e2)
-            pk[e2] = pack_bf16(__uint_as_float(o[2 * e2]) * inv_l,
-                               __uint_as_float(o[2 * e2 + 1]) * inv_l);
-          if (row_ok) {
-#pragma unroll
-            for (int v = 0; v < 4; ++v)
-              orow[(q2 * 2 + half) * 4 + v] =
-                  make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-          }
-        }
+      // the output is written once the next item is set up (or at the end),
+      // so that the item's last P V runs meanwhile
+      pend = true;
+      pend_l = l;
+      if (!kDefer) {
+        ok = finish(seq);
+        if (!ok) break;
       }
-      tc_fence_before();
-      mbar_arrive(bar(B_IEMPTY + slot));
     }
     if (!ok && lane == 0) {
       *abort = 1;
@@ -971,12 +1113,12 @@ EncodeTiledFn encode_fn() {
 
 // [planes, n, 128] bf16 viewed as a 3-D tensor with 64 x 128 x 1 boxes and
 // 128-byte swizzle; rows past n read as zeros.
-bool make_map(CUtensorMap* map, const void* base, int64_t planes, int64_t n) {
+bool make_map(CUtensorMap* map, const void* base, int64_t planes, int64_t n, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)HD, (cuuint64_t)n, (cuuint64_t)planes};
   const cuuint64_t strides[2] = {(cuuint64_t)HD * 2, (cuuint64_t)n * HD * 2};
-  const cuuint32_t box[3] = {64, (cuuint32_t)BM, 1};
+  const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -996,37 +1138,60 @@ cudaError_t launch_variant(const CUtensorMap& mq, const CUtensorMap& mk,
   return cudaGetLastError();
 }
 
+// Largest s kept in registers: each thread holds its row's bin starts (and,
+// without the causal mask, the bin ends).
+constexpr int kSregCausal = 16;
+constexpr int kSregFull = 16;
+int sreg_for(int s, int causal, int exact) {
+  if (exact) return 0;
+  const int lim = causal ? kSregCausal : kSregFull;
+  return s <= lim ? lim : 0;
+}
+
+constexpr size_t kSmemLimit = 232448;   // opt-in dynamic shared memory per CTA
+
+size_t smem_for(int slots, bool out, int s, int causal, int exact) {
+  const int sreg = sreg_for(s, causal, exact);
+  return 1024 + OFF_KV + (size_t)slots * kTileBytes + (out ? kOutBytes : 0) +
+         bp_bytes(s, exact != 0, causal != 0, sreg) + stage_bytes(s, exact != 0) +
+         sizeof(Ctl);
+}
+
+// Three K/V slots; the output staging buffer when the per-row bin lists
+// leave room for it (else the epilogue stores its rows directly).
+constexpr int kSlots = 3;
+bool out_staged(int s, int causal, int exact) {
+  return smem_for(kSlots, true, s, causal, exact) <= kSmemLimit;
+}
 }  // namespace
 
-constexpr int kSreg = 16;
-
 size_t attn_tc_smem_bytes(int s, int causal, int exact) {
-  const int sreg = (!exact && s <= kSreg) ? kSreg : 0;
-  return 1024 + OFF_BP + bp_bytes(s, exact != 0, causal != 0, sreg) +
-         stage_bytes(s, exact != 0) + sizeof(Ctl);
+  return smem_for(kSlots, out_staged(s, causal, exact), s, causal, exact);
 }
 
 cudaError_t launch_attn_tc(const AttnArgs& a, const float* slopes_host,
                            int num_sms, cudaStream_t st) {
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, a.Q, (int64_t)a.B * a.Hq, a.n) ||
-      !make_map(&mk, a.K, (int64_t)a.B * a.Hkv, a.n) ||
-      !make_map(&mv, a.V, (int64_t)a.B * a.Hkv, a.n))
+  if (!make_map(&mq, a.Q, (int64_t)a.B * a.Hq, a.n, BM) ||
+      !make_map(&mk, a.K, (int64_t)a.B * a.Hkv, a.n, BN) ||
+      !make_map(&mv, a.V, (int64_t)a.B * a.Hkv, a.n, BN))
     return cudaErrorInvalidValue;
   TcParams p;
   p.a = a;
   for (int h = 0; h < 512; ++h)
     p.slope_log2[h] = (slopes_host && h < a.Hq) ? slopes_host[h] : 0.f;
   p.QT = (a.n + BM - 1) / BM;
+  p.slots = kSlots;
+  p.out_smem = out_staged(a.s, a.causal, a.exact) ? 1 : 0;
   const int grid = a.num_items < num_sms ? a.num_items : num_sms;
   const size_t smem = attn_tc_smem_bytes(a.s, a.causal, a.exact);
   if (a.exact) {
     return a.causal ? launch_variant<true, true, 0>(mq, mk, mv, p, smem, grid, st)
                     : launch_variant<true, false, 0>(mq, mk, mv, p, smem, grid, st);
   }
-  if (a.s <= kSreg) {
-    return a.causal ? launch_variant<false, true, kSreg>(mq, mk, mv, p, smem, grid, st)
-                    : launch_variant<false, false, kSreg>(mq, mk, mv, p, smem, grid, st);
+  if (sreg_for(a.s, a.causal, 0) > 0) {
+    return a.causal ? launch_variant<false, true, kSregCausal>(mq, mk, mv, p, smem, grid, st)
+                    : launch_variant<false, false, kSregFull>(mq, mk, mv, p, smem, grid, st);
   }
   return a.causal ? launch_variant<false, true, 0>(mq, mk, mv, p, smem, grid, st)
                   : launch_variant<false, false, 0>(mq, mk, mv, p, smem, grid, st);
