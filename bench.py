@@ -146,16 +146,43 @@ def kernel_traffic():
     """dram bytes per launch of the fused kernel from the committed ncu summary,
     valid only for the exact kernel source it was taken from."""
     path = os.path.join(ROOT, "profiles", "attn_tc_traffic.json")
-    src = os.path.join(ROOT, "positional_lsh_approximation_gb300", "csrc", "attn_tc.cu")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
-    with open(src, "rb") as f:
-        digest = hashlib.sha256(f.read()).hexdigest()[:16]
-    if d.get("source_sha256_16") != digest:
+    if d.get("source_sha256_16") != kernel_source_digest():
         return None
     return d.get("traffic_bytes_per_launch")
+
+
+KERNEL_SOURCES = ("attn_tc.cu", "tc_ptx.cuh", "bins_dev.cuh", "plsh_internal.h")
+
+
+def kernel_source_digest() -> str:
+    """sha256 (16 hex digits) over the fused kernel's source files."""
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "positional_lsh_approximation_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+# ------------------------------------------------------ cross-rank timing
+def max_over_ranks(x: float, device=None) -> float:
+    """Largest x over the ranks of the default process group (x itself when
+    there is none): the job is as slow as its slowest replica."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: int, world: int, steps: int, total_ms: float) -> float:
+    """Units processed by all replicas per second over the slowest rank's time."""
+    return units_per_rank * world * steps / (total_ms / 1e3)
 
 
 # ------------------------------------------------------------- our arm
@@ -207,13 +234,8 @@ def run_ours(args, rank, world):
     step_ms = [a.elapsed_time(c) for a, b, c in ev]
     attn_ms = [b.elapsed_time(c) for a, b, c in ev]
     sample_ms = [a.elapsed_time(b) for a, b, c in ev]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    tokens = w.B * w.n * world
-    value = tokens * args.steps / (total_ms / 1e3)
+    total_ms = max_over_ranks(sum(step_ms), dev)
+    value = whole_job_rate(w.B * w.n, world, args.steps, total_ms)
     attn_avg_s = statistics.mean(attn_ms) / 1e3
 
     # end to end through the public API with host buffers (pinned)
