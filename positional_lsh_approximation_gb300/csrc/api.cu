@@ -149,13 +149,18 @@ plsh_status check_bins_device(const plsh_bins* b) {
 }
 
 plsh_status resample(plsh_bins* b, const double* sigma, uint64_t seed, cudaStream_t st) {
-  b->sigma_host.assign(sigma, sigma + b->H);
-  order_heads(b);
-  PLSH_TRY_CUDA(cudaMemcpyAsync(b->d_sigma, sigma, sizeof(double) * b->H,
-                                cudaMemcpyHostToDevice, st), "copy sigma");
-  PLSH_TRY_CUDA(cudaMemcpyAsync(b->d_head_order, b->head_order.data(),
-                                sizeof(int32_t) * b->H, cudaMemcpyHostToDevice, st),
-                "copy head order");
+  // sigma and the head order live on the device; they are uploaded again only
+  // when sigma changes (a redraw with new seeds alone launches one kernel)
+  if (!b->sigma_on_device || !std::equal(sigma, sigma + b->H, b->sigma_host.begin())) {
+    b->sigma_host.assign(sigma, sigma + b->H);
+    order_heads(b);
+    PLSH_TRY_CUDA(cudaMemcpyAsync(b->d_sigma, sigma, sizeof(double) * b->H,
+                                  cudaMemcpyHostToDevice, st), "copy sigma");
+    PLSH_TRY_CUDA(cudaMemcpyAsync(b->d_head_order, b->head_order.data(),
+                                  sizeof(int32_t) * b->H, cudaMemcpyHostToDevice, st),
+                  "copy head order");
+    b->sigma_on_device = true;
+  }
   PLSH_TRY_CUDA(plsh::launch_sample(b, seed, st), "sampler launch");
   return PLSH_OK;
 }

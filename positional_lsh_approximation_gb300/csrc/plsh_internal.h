@@ -62,6 +62,7 @@ struct plsh_bins {
   int32_t* d_head_order = nullptr;   // [H]
   std::vector<double> sigma_host;    // per-head scale (drawn or estimated)
   std::vector<int32_t> head_order;   // heads by expected work, descending
+  bool sigma_on_device = false;      // d_sigma / d_head_order hold sigma_host
 };
 
 namespace plsh {

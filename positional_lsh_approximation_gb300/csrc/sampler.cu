@@ -18,6 +18,7 @@
 // bin starts plus the neighbouring starts), which the attention kernels read
 // to find each row's bin in O(1).
 #include <cuda_runtime.h>
+#include <limits.h>
 #include <stdint.h>
 
 #include <algorithm>
@@ -82,8 +83,8 @@ __device__ double ln_rn(double x) {
 }
 
 // ceil(u + k w) with the multiply and the add rounded separately.
-__device__ __forceinline__ double start_of(long long k, double w, double u) {
-  return ceil(__dadd_rn(u, __dmul_rn((double)k, w)));
+__device__ __forceinline__ long long start_of(long long k, double w, double u) {
+  return __double2ll_ru(__dadd_rn(u, __dmul_rn((double)k, w)));   // ceil, as an integer
 }
 
 // One thread per listed start (terminal entries excluded): set its bit.
@@ -224,7 +225,7 @@ sample_kernel(int64_t n, int64_t W, int nseg, int spc, int s,
   __shared__ uint32_t bits_s[kSegWords];
   __shared__ int32_t warp_buf[kSampThreads / 32];
   __shared__ int32_t next_s, prev_s;
-  __shared__ long long k0_s;
+  __shared__ long long k0_s, k1_s;
   if (threadIdx.x < 2) {
     const int h = hs / s, t = hs % s;
     uint32_t c[4] = {(uint32_t)t, (uint32_t)h, 0u, 0u};
@@ -256,10 +257,18 @@ sample_kernel(int64_t n, int64_t W, int nseg, int spc, int s,
     if (threadIdx.x == 0) {
       next_s = (int32_t)n;
       prev_s = P0 > 0 ? 0 : -1;    // position 0 always opens a bin
-      // first k whose start can reach the segment: just below
-      // (P0 - 1 - u) / w, stepped back two to absorb rounding
-      const double est = w >= 1.0 ? floor(((double)(P0 - 1) - u) / w) - 2.0 : 0.0;
-      k0_s = est > 0.0 ? (long long)est : 0ll;
+      // k range of the walk, from just below the first start that can reach
+      // the segment to just past the first start at or beyond P1; estimated
+      // in fp32 (no fp64 division) with a slack that covers its rounding
+      if (w >= 1.0) {
+        const float wf = (float)w, uf = (float)u;
+        const float ka = ((float)(P0 - 1) - uf) / wf;
+        const float kb = ((float)P1 - uf) / wf;
+        const float slack = 2.0f + fmaxf(fabsf(ka), fabsf(kb)) * 0x1p-18f;
+        const float lo = floorf(ka - slack), hi = ceilf(kb + slack);
+        k0_s = lo > 0.0f ? (long long)lo : 0ll;
+        k1_s = hi > 0.0f ? (long long)hi : 0ll;
+      }
     }
     __syncthreads();
     if (w < 1.0) {   // every position opens a bin
@@ -274,23 +283,24 @@ sample_kernel(int64_t n, int64_t W, int nseg, int spc, int s,
       }
     } else {
       if (P0 == 0 && threadIdx.x == 0) atomicOr(&bits_s[0], 1u);
-      // k from k0 while the exact start stays below P1; starts below P0 give
-      // the last start before the segment, the first at or past P1 the next
-      const long long k0 = k0_s;
-      int32_t before = -1;
-      for (long long k = k0 + threadIdx.x;; k += kSampThreads) {
-        const double c = start_of(k, w, u);
-        if (c >= (double)P1) {
-          if (c < (double)n) atomicMin(&next_s, (int32_t)c);
-          break;
-        }
-        if (c >= (double)P0) {
-          const int64_t off = (int64_t)c - P0;
+      // every k of the range (no data-dependent exit, so the loads of
+      // independent k overlap): starts below P0 give the last start before
+      // the segment, the smallest at or past P1 the next one
+      const long long k0 = k0_s, k1 = k1_s;
+      int32_t before = -1, after = INT_MAX;
+#pragma unroll 4
+      for (long long k = k0 + threadIdx.x; k <= k1; k += kSampThreads) {
+        const long long c = start_of(k, w, u);
+        if (c >= P1) {
+          if (c < n) after = min(after, (int32_t)c);
+        } else if (c >= P0) {
+          const int64_t off = c - P0;
           atomicOr(&bits_s[off >> 5], 1u << (off & 31));
         } else {
           before = max(before, (int32_t)c);
         }
       }
+      if (after != INT_MAX) atomicMin(&next_s, after);
       if (before >= 0) atomicMax(&prev_s, before);
     }
     __syncthreads();

@@ -81,6 +81,14 @@ def test_sampler_bit_exact(n, H, s, sig, seed):
     off2, st2 = bins.to_host()
     roff2, rst2 = oracle.sample_bins(n, sigma * 1.5, s, seed + 1)
     assert np.array_equal(off2, roff2) and np.array_equal(st2, rst2)
+    # same sigma, new seed (sigma stays on the device), then back to the first
+    bins.resample(sigma * 1.5, seed + 2)
+    off3, st3 = bins.to_host()
+    roff3, rst3 = oracle.sample_bins(n, sigma * 1.5, s, seed + 2)
+    assert np.array_equal(off3, roff3) and np.array_equal(st3, rst3)
+    bins.resample(sigma, seed)
+    off4, st4 = bins.to_host()
+    assert np.array_equal(off4, roff) and np.array_equal(st4, rst)
     bins.free()
 
 
