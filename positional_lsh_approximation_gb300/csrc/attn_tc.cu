@@ -38,11 +38,12 @@
 //               per row, tcgen05.ld of the score row, running max over the
 //               valid keys, lazy rescale of O in TMEM (only when the max grows
 //               by more than 2^8), P = c 2^(x - m) split into two bf16 terms
-//               P_hi + P_lo written back over the consumed score columns,
+//               P_hi + P_lo (truncated head, rounded remainder) written back
+//               over the consumed score columns,
 //               fp32 row sums, and the O / l epilogue.
 //   O += P_hi V + P_lo V runs as two tensor-core products with A read from
 //   TMEM: a single bf16 P carries a 2^-9 relative error per weight, which
-//   shows in rows whose few keys cancel; the pair carries about 2^-17.
+//   shows in rows whose few keys cancel; the pair carries about 2^-16.
 // TMEM columns: S_A | S_B | O_A | O_B.  Every wait on an mbarrier is bounded;
 // on expiry the CTA raises the library error flag, drains its in-flight copies
 // and MMAs, frees TMEM and exits.
@@ -1032,15 +1033,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                 scale_by_planes<2, CAUSAL>(pv, base, up, dn);
               }
             }
+            // P_hi: the upper 16 bits of each weight (truncation, so that
+            // P - P_hi is exact in fp32); P_lo: that remainder rounded to
+            // bf16, relative error below 2^-16 for the pair
 #pragma unroll
             for (int e2 = 0; e2 < 16; ++e2) {
               const uint64_t p2 = f2_pack(pv[2 * e2], pv[2 * e2 + 1]);
               lsum2 = f2_add(lsum2, p2);
-              const uint32_t hp = pack_bf16(pv[2 * e2], pv[2 * e2 + 1]);
+              const uint32_t b0 = __float_as_uint(pv[2 * e2]), b1 = __float_as_uint(pv[2 * e2 + 1]);
               float l0, l1;
-              f2_unpack(f2_sub(p2, f2_pack(__uint_as_float(hp << 16),
-                                           __uint_as_float(hp & 0xffff0000u))), l0, l1);
-              hi[e2] = hp;
+              f2_unpack(f2_sub(p2, f2_pack(__uint_as_float(b0 & 0xffff0000u),
+                                           __uint_as_float(b1 & 0xffff0000u))), l0, l1);
+              hi[e2] = __byte_perm(b0, b1, 0x7632);
               lo[e2] = pack_bf16(l0, l1);
             }
           }
