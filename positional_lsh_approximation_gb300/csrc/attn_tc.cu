@@ -289,6 +289,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // launched as a programmatic dependent of the kernel before it (the
+  // sampler): the set-up above overlaps its tail; nothing in global memory
+  // is read or written before that kernel has completed
+  grid_dep_wait();
   const uint32_t tmem = ctl->tmem_base;
   const int n = a.n, Hq = a.Hq, Hkv = a.Hkv;
 
@@ -1138,8 +1142,19 @@ cudaError_t launch_variant(const CUtensorMap& mq, const CUtensorMap& mk,
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, smem, st>>>(mq, mk, mv, p);
-  return cudaGetLastError();
+  // programmatic stream serialization: the CTAs may start (and set up
+  // shared memory, barriers and TMEM) while the previous kernel finishes
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, p);
 }
 
 // Largest s kept in registers: each thread holds its row's bin starts (and,

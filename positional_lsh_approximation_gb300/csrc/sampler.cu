@@ -226,6 +226,9 @@ sample_kernel(int64_t n, int64_t W, int nseg, int spc, int s,
   __shared__ int32_t warp_buf[kSampThreads / 32];
   __shared__ int32_t next_s, prev_s;
   __shared__ long long k0_s, k1_s;
+  // the attention kernel that follows may start its set-up now; it waits
+  // for this grid's completion before it reads the records
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x < 2) {
     const int h = hs / s, t = hs % s;
     uint32_t c[4] = {(uint32_t)t, (uint32_t)h, 0u, 0u};
