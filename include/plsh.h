@@ -68,9 +68,10 @@ typedef struct plsh_bins plsh_bins;
  * seed, counter = (t, h, 0, 0)) gives U0, U1, U2 = (x + 0.5) 2^-32; the width
  * is w = sigma_h (-ln U0 - ln U1) ~ Gamma(shape 2, scale sigma_h) and the
  * offset u = w U2 ~ U(0, w).  Bin starts are 0 and ceil(u + k w) for
- * k = 0, 1, ... below n (every position its own bin when w < 1).  The
- * arithmetic is fp64 with each operation rounded separately, so the starts
- * agree bit for bit with any other implementation of the same recipe.
+ * k = 0, 1, ... below n, u + k w one fused multiply-add (every position its
+ * own bin when w < 1).  The arithmetic is fp64, each operation (a fused
+ * multiply-add counts as one) rounded once, so the starts agree bit for bit
+ * with any other implementation of the same recipe.
  *
  *   n        sequence length, 1 <= n < 2^31
  *   sigma_h  host array [H], each finite and > 0 (sigma = 1 / ALiBi slope)

@@ -27,11 +27,13 @@
  *     counter = (t, h, 0, 0), uniforms (x + 0.5) * 2^-32;
  *   - width w = sigma * (E1 + E2) with E = -ln U  ->  Gamma(shape 2, scale
  *     sigma); offset u = w * U3  ->  U(0, w);
- *   - bin starts: 0, then ceil(u + k*w) for k = 0, 1, ... below n,
- *     de-duplicated; all singletons when w < 1;
+ *   - bin starts: 0, then ceil(u + k*w) for k = 0, 1, ... below n, with
+ *     u + k*w one fused multiply-add (rounded once), de-duplicated; all
+ *     singletons when w < 1;
  *   - ln is this file's own atanh-series logarithm built from correctly
- *     rounded +, -, *, / only, so that another implementation of the same
- *     recipe reproduces the widths bit for bit.
+ *     rounded +, -, *, / and fused multiply-add (Horner steps) only, so that
+ *     another implementation of the same recipe reproduces the widths bit
+ *     for bit.
  *
  * Build: gcc -O2 -fopenmp -ffp-contract=off (no fast-math).  fp contraction
  * must stay off: the sampler's arithmetic is defined operation by operation.
@@ -103,15 +105,13 @@ double oracle_ln64(double x) {
   double poly = 1.0 / (double)(2 * ORACLE_LN_TERMS + 1);
   for (int k = ORACLE_LN_TERMS - 1; k >= 0; --k) {
     double ck = 1.0 / (double)(2 * k + 1);
-    double t = poly * z2;
-    poly = t + ck;
+    poly = fma(poly, z2, ck);     /* one rounding per step */
   }
   double two_z = z + z;
   double ln_m = two_z * poly;
   double ed = (double)e;
-  double hi = ed * ORACLE_LN2_HI;
-  double lo = ed * ORACLE_LN2_LO;
-  double tail = lo + ln_m;
+  double hi = ed * ORACLE_LN2_HI;            /* exact */
+  double tail = fma(ed, ORACLE_LN2_LO, ln_m);
   return hi + tail;
 }
 
@@ -152,8 +152,7 @@ int64_t oracle_bins_one(int64_t n, double w, double u, int32_t* starts,
   double last = 0.0;
   const double nd = (double)n;
   for (int64_t k = 0;; ++k) {
-    double kw = (double)k * w;
-    double p = u + kw;
+    double p = fma((double)k, w, u);   /* u + k w, rounded once */
     double c = ceil(p);
     if (c >= nd) break;
     if (c > last) {

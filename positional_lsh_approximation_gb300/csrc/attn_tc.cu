@@ -698,13 +698,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         int lomin = INT_MAX, himax = 0;
         lomax = INT_MIN;
         himin = INT_MAX;
+        // every record is loaded first (a clamped index, so that no load
+        // waits behind a branch), then the bins are found
+        uint4 rec_r[SREG > 0 ? SREG : 1];
+        const uint32_t rs_addr = smem_u32(rs);
+#pragma unroll
+        for (int t = 0; t < (SREG > 0 ? SREG : 1); ++t)
+          rec_r[t] = ld_shared_v4(rs_addr + (uint32_t)min(t, s - 1) * (kWordsPerTile * 16u));
 #pragma unroll
         for (int t = 0; t < (SREG > 0 ? SREG : 1); ++t) {
           int lo = INT_MAX, hi = INT_MAX;
           if (t < s) {
-            const BinRecord rc = unpack_record(rs[t * kWordsPerTile]);
+            const BinRecord rc = unpack_record(rec_r[t]);
             lo = bin_lo(rc, ii);
-            hi = bin_hi(rc, ii);
+            if (!CAUSAL) hi = bin_hi(rc, ii);
             lomin = min(lomin, lo);
             lomax = max(lomax, lo);
             himax = max(himax, hi);

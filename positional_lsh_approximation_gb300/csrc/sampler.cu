@@ -8,11 +8,12 @@
 //   U_k = (x_k + 0.5) 2^-32
 //   w = sigma_h (-ln U0 - ln U1)   ~ Gamma(shape 2, scale sigma_h)
 //   u = w U2                        ~ U(0, w)
-//   bin starts: 0 and ceil(u + k w), k = 0, 1, ... below n (all positions
-//   when w < 1).
+//   bin starts: 0 and ceil(u + k w), k = 0, 1, ... below n, u + k w one
+//   fused multiply-add (all positions when w < 1).
 // All fp64 arithmetic is done one correctly rounded operation at a time
-// (__dadd_rn etc.), with the library's own logarithm, so the boundaries are
-// reproducible bit for bit by any implementation of the same recipe.
+// (__dadd_rn, __fma_rn etc.), with the library's own logarithm, so the
+// boundaries are reproducible bit for bit by any implementation of the same
+// recipe.
 //
 // Output layout: for every hash, one BinRecord per 32 positions (bitmap of
 // bin starts plus the neighbouring starts), which the attention kernels read
@@ -53,7 +54,8 @@ __device__ __forceinline__ void philox4x32_10(uint32_t c[4], uint32_t k0,
 
 // Natural log of a positive normal double: x = 2^e m, m reduced to
 // [sqrt(1/2), sqrt(2)), ln m = 2 atanh(z) = 2 z sum_k z^2k / (2k+1) with
-// z = (m-1)/(m+1), 12 terms by Horner, then e ln2 added in two parts
+// z = (m-1)/(m+1), 12 terms by Horner with fused multiply-adds, then e ln2
+// added in two parts
 // (ln2 split so that e * hi is exact).
 __device__ double ln_rn(double x) {
   const double kLn2Hi = 0x1.62e42fef00000p-1;
@@ -75,16 +77,16 @@ __device__ double ln_rn(double x) {
   const double z2 = __dmul_rn(z, z);
   double poly = kInvOdd[11];
 #pragma unroll
-  for (int k = 10; k >= 0; --k) poly = __dadd_rn(__dmul_rn(poly, z2), kInvOdd[k]);
+  for (int k = 10; k >= 0; --k) poly = __fma_rn(poly, z2, kInvOdd[k]);
   const double ln_m = __dmul_rn(__dadd_rn(z, z), poly);
   const double ed = (double)e;
-  return __dadd_rn(__dmul_rn(ed, kLn2Hi),
-                   __dadd_rn(__dmul_rn(ed, kLn2Lo), ln_m));
+  return __dadd_rn(__dmul_rn(ed, kLn2Hi),          // exact product
+                   __fma_rn(ed, kLn2Lo, ln_m));
 }
 
 // ceil(u + k w) with the multiply and the add rounded separately.
 __device__ __forceinline__ long long start_of(long long k, double w, double u) {
-  return __double2ll_ru(__dadd_rn(u, __dmul_rn((double)k, w)));   // ceil, as an integer
+  return __double2ll_ru(__fma_rn((double)k, w, u));   // ceil(u + k w), rounded once
 }
 
 // One thread per listed start (terminal entries excluded): set its bit.
