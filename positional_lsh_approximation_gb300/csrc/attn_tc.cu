@@ -1164,14 +1164,19 @@ cudaError_t launch_variant(const CUtensorMap& mq, const CUtensorMap& mk,
   return cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, p);
 }
 
-// Largest s kept in registers: each thread holds its row's bin starts (and,
-// without the causal mask, the bin ends).
-constexpr int kSregCausal = 16;
-constexpr int kSregFull = 16;
+// Register slots for the rows' bin starts (and, without the causal mask,
+// ends): the smallest compiled size that holds s, so that no slot is padding
+// the per-chunk count walks over; sorted lists in shared memory beyond.
 int sreg_for(int s, int causal, int exact) {
   if (exact) return 0;
-  const int lim = causal ? kSregCausal : kSregFull;
-  return s <= lim ? lim : 0;
+  if (causal) {
+    for (int r : {4, 8, 10, 12, 16})
+      if (s <= r) return r;
+    return 0;
+  }
+  for (int r : {8, 16})
+    if (s <= r) return r;
+  return 0;
 }
 
 constexpr size_t kSmemLimit = 232448;   // opt-in dynamic shared memory per CTA
@@ -1215,9 +1220,15 @@ cudaError_t launch_attn_tc(const AttnArgs& a, const float* slopes_host,
     return a.causal ? launch_variant<true, true, 0>(mq, mk, mv, p, smem, grid, st)
                     : launch_variant<true, false, 0>(mq, mk, mv, p, smem, grid, st);
   }
-  if (sreg_for(a.s, a.causal, 0) > 0) {
-    return a.causal ? launch_variant<false, true, kSregCausal>(mq, mk, mv, p, smem, grid, st)
-                    : launch_variant<false, false, kSregFull>(mq, mk, mv, p, smem, grid, st);
+  switch (a.causal ? sreg_for(a.s, 1, 0) : -sreg_for(a.s, 0, 0)) {
+    case 4: return launch_variant<false, true, 4>(mq, mk, mv, p, smem, grid, st);
+    case 8: return launch_variant<false, true, 8>(mq, mk, mv, p, smem, grid, st);
+    case 10: return launch_variant<false, true, 10>(mq, mk, mv, p, smem, grid, st);
+    case 12: return launch_variant<false, true, 12>(mq, mk, mv, p, smem, grid, st);
+    case 16: return launch_variant<false, true, 16>(mq, mk, mv, p, smem, grid, st);
+    case -8: return launch_variant<false, false, 8>(mq, mk, mv, p, smem, grid, st);
+    case -16: return launch_variant<false, false, 16>(mq, mk, mv, p, smem, grid, st);
+    default: break;
   }
   return a.causal ? launch_variant<false, true, 0>(mq, mk, mv, p, smem, grid, st)
                   : launch_variant<false, false, 0>(mq, mk, mv, p, smem, grid, st);

@@ -112,6 +112,12 @@ SMALL = [
     ("bf16_s48", 1, 2, 2, 640, 128, "bf16", True, 48, (2.0, 30.0)),
     ("bf16_s64", 1, 2, 2, 640, 128, "bf16", True, 64, (2.0, 30.0)),
     ("bf16_noncausal_s30", 1, 2, 1, 400, 128, "bf16", False, 30, (0.8, 40.0)),
+    # every register-slot variant of the fused kernel (s rounded up to 4, 8,
+    # 10, 12 or 16 causal; 8 or 16 without the causal mask)
+    ("bf16_s7", 1, 2, 1, 900, 128, "bf16", True, 7, (2.5, 90.0)),
+    ("bf16_s12", 2, 2, 1, 600, 128, "bf16", True, 12, (1.5, 20.0)),
+    ("bf16_s15", 1, 4, 2, 520, 128, "bf16", True, 15, (1.1, 4.0, 30.0, 700.0)),
+    ("bf16_noncausal_s13", 1, 2, 1, 450, 128, "bf16", False, 13, (2.0, 70.0)),
     ("bf16_short", 1, 3, 1, 70, 128, "bf16", True, 3, (1.0, 8.0, 1e5)),
     ("bf16_one_token", 1, 2, 1, 1, 128, "bf16", True, 2, (4.0, 4.0)),
 ]
