@@ -380,10 +380,23 @@ def cpu_baseline(w, Qn, Kn, Vn, offsets, starts, budget_s):
         if elapsed >= budget_s or done >= w.B * w.n:
             break
         npos = int(min(4096, max(npos * 2, npos * (budget_s - elapsed) / max(dt, 1e-3) * 0.5)))
-    return {"value": done / elapsed, "unit": "tokens/s", "cores": oracle.max_threads(),
+    all_cores = oracle.max_threads()
+    # the same oracle on one core, over a smaller sample
+    oracle.set_threads(1)
+    pos = rng.integers(0, w.n, size=max(1, min(256, done // 16))).astype(np.int32)
+    t0 = time.perf_counter()
+    oracle.plsh_attn_rows(Qn, Kn, Vn, offsets, starts, w.s, w.causal,
+                          (np.zeros(pos.size * w.Hq, np.int32),
+                           np.repeat(np.arange(w.Hq, dtype=np.int32), pos.size),
+                           np.tile(pos, w.Hq)))
+    one_core = pos.size / (time.perf_counter() - t0)
+    oracle.set_threads(cores)
+    return {"value": done / elapsed, "unit": "tokens/s", "cores": all_cores,
             "kind": "oracle",
             "sample": f"{done} random token positions x all {w.Hq} heads of batch 0, "
-                      f"fp64, {elapsed:.1f} s"}
+                      f"fp64, {elapsed:.1f} s",
+            "one_core": {"value": one_core, "unit": "tokens/s",
+                         "sample": f"{pos.size} random token positions x all {w.Hq} heads"}}
 
 
 def run_reference(args, rank, world):
