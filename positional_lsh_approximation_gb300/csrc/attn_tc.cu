@@ -1039,7 +1039,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
               } else if (!multi) {
                 scale_by_steps<CAUSAL>(pv, base, up[0], dn[0]);
               } else if (__any_sync(FULL, (up[2] | up[3] | up[4] | dn[2] | dn[3] | dn[4]) != 0u)) {
-                scale_by_planes<5, CAUSAL>(pv, base, up, dn);
+                // a multiplicity never exceeds the number of register slots
+                scale_by_planes<(SREG == 0 || SREG > 15) ? 5 : (SREG > 7 ? 4 : 3), CAUSAL>(
+                    pv, base, up, dn);
               } else {
                 scale_by_planes<2, CAUSAL>(pv, base, up, dn);
               }
