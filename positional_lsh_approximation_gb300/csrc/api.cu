@@ -36,10 +36,15 @@ constexpr int kMaxDevices = 64;
 std::mutex g_ctx_mu;
 plsh::DeviceCtx g_ctx[kMaxDevices];
 
-bool fault_oom() {
+// Fault injection for the tests, from the environment: PLSH_FAULT=oom fails
+// every device allocation; PLSH_FAULT=stall makes the next tensor-core
+// attention publish no work item, so every device-side wait runs out (with
+// nothing in flight) and the error flag reports PLSH_ERR_TIMEOUT.
+bool fault_is(const char* what) {
   const char* f = getenv("PLSH_FAULT");
-  return f != nullptr && strcmp(f, "oom") == 0;
+  return f != nullptr && strcmp(f, what) == 0;
 }
+bool fault_oom() { return fault_is("oom"); }
 
 plsh_status dev_alloc(void** p, size_t bytes, const char* what) {
   if (fault_oom()) return fail(PLSH_ERR_NOMEM, std::string(what) + ": injected allocation failure");
@@ -352,6 +357,7 @@ plsh_status run_attention(const plsh_tensor* Q, const plsh_tensor* K, const plsh
   }
   a.err = ctx->d_err;
   a.wait_ns = ctx->wait_ns;
+  a.stall = fault_is("stall") ? 1 : 0;
   {
     std::lock_guard<std::mutex> lk(g_ctx_mu);
     a.queue = ctx->d_queue + 2 * (ctx->slot_counter++ % plsh::kQueueSlots);

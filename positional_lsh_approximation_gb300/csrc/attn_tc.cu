@@ -301,7 +301,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
     // pops items, stages the rows' bin records, finds the key envelope and
     // publishes the item up to kRing - 1 items ahead of its consumers
     bool ok = true;
-    for (int seq = 0;; ++seq) {
+    for (int seq = 0; !a.stall; ++seq) {   // stall: fault injection
       const int slot = seq % kRing;
       const uint32_t use = (uint32_t)(seq / kRing);
       int idx = 0;

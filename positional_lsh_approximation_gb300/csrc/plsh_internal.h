@@ -92,6 +92,7 @@ struct AttnArgs {
   int* err;
   int* queue;                      // {next item, finished CTAs}
   uint64_t wait_ns;
+  int stall;                       // fault injection: the scheduler publishes no item
 };
 
 // attn_simt.cu (CUDA cores, any dtype, d in {64, 128})
