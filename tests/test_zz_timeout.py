@@ -44,3 +44,16 @@ def test_stalled_kernel_reports_timeout_and_context_recovers(monkeypatch):
     plsh.stream_status()
     assert torch.equal(again, ref)
     bins.free()
+
+
+def test_injected_allocation_failure_is_reported(monkeypatch):
+    plsh.build()
+    sigma = np.array([3.0, 30.0])
+    monkeypatch.setenv("PLSH_FAULT", "oom")
+    with pytest.raises(plsh.PlshError) as err:
+        plsh.sample_bins(1000, sigma, 4, seed=1)
+    assert err.value.status == plsh.PLSH_ERR_NOMEM
+    monkeypatch.delenv("PLSH_FAULT")
+    bins = plsh.sample_bins(1000, sigma, 4, seed=1)
+    assert bins.shape() == (1000, 2, 4)
+    bins.free()
