@@ -183,6 +183,29 @@ plsh_status plsh_alibi_attn_noalloc(const plsh_tensor* Q, const plsh_tensor* K,
                                     int32_t causal, plsh_tensor* O, void* stream);
 
 /*
+ * plsh_alibi_attn_host -- plsh_alibi_attn on tensors in host memory.  The
+ * paper has no counterpart: this is a deployment variant, not part of the
+ * method.
+ *
+ * Q, K, V and O follow the plsh_alibi_attn rules except that their `data`
+ * are host pointers (page-locked memory lets the copies run asynchronously
+ * and overlap; pageable memory works but each copy then blocks the calling
+ * thread).  The library stages the tensors through device buffers it keeps
+ * per device (grown on demand, which synchronises the device; held until the
+ * process exits) and splits the query rows into up to four chunks on the
+ * tensor-core path: chunk c + 1 is copied in and chunk c - 1 copied out, on
+ * two copy streams of its own, while the fused kernel runs on chunk c (with
+ * the causal mask only the keys up to a chunk's last row are needed before
+ * it starts).  The call returns once everything is queued; O is complete on
+ * the host when `stream` reaches the point of the call (synchronise it before
+ * reading O).  Calls on one device share the staging buffers: issue them on
+ * one stream, or order their streams.
+ */
+plsh_status plsh_alibi_attn_host(const plsh_tensor* Q, const plsh_tensor* K,
+                                 const plsh_tensor* V, const plsh_bins* bins, int32_t causal,
+                                 plsh_tensor* O, void* stream);
+
+/*
  * plsh_alibi_exact -- exact ALiBi attention T* (the dense comparator, Problem
  * statement: O(n^2) in the bias matrix):
  *   O_i = sum_j e^{S_ij - |i-j|/sigma_h} v_j / sum_j e^{S_ij - |i-j|/sigma_h}

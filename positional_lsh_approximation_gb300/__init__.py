@@ -21,7 +21,7 @@ import torch
 from . import build as _build_mod
 
 __all__ = ["build", "load", "sample_bins", "bins_from_host", "Bins", "alibi_attn",
-           "alibi_attn_noalloc",
+           "alibi_attn_noalloc", "alibi_attn_host",
            "alibi_exact", "stream_status", "set_wait_limit_ns", "PlshError",
            "library_path"]
 
@@ -80,6 +80,7 @@ def load():
             "plsh_bins_draws": [P, D, D, P],
             "plsh_alibi_attn": [TP, TP, TP, P, I32, TP, P],
             "plsh_alibi_attn_noalloc": [TP, TP, TP, P, I32, TP, P],
+            "plsh_alibi_attn_host": [TP, TP, TP, P, I32, TP, P],
             "plsh_alibi_exact": [TP, TP, TP, D, I32, TP, P],
             "plsh_stream_status": [P],
             "plsh_set_wait_limit_ns": [U64],
@@ -214,6 +215,25 @@ def _desc(t: torch.Tensor) -> _Tensor:
     return _Tensor(t.data_ptr(), _DT[t.dtype], B, H, n, d)
 
 
+def _desc_host(t: torch.Tensor) -> _Tensor:
+    if t.device.type != "cpu":
+        raise ValueError("host-buffer call: tensors must be in host memory")
+    return _desc(t)
+
+
+def alibi_attn_host(Q, K, V, bins: Bins, causal: bool, out=None, stream=None):
+    """plsh_alibi_attn_host: Q, K, V (and out) in host memory, preferably
+    page-locked; the copies in and out overlap the kernel.  `out` is complete
+    once `stream` is synchronised."""
+    if out is None:
+        out = torch.empty(Q.shape, dtype=Q.dtype, pin_memory=torch.cuda.is_available())
+    tq, tk, tv, to = _desc_host(Q), _desc_host(K), _desc_host(V), _desc_host(out)
+    _check(load().plsh_alibi_attn_host(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv),
+                                       bins.handle, int(bool(causal)), ctypes.byref(to),
+                                       _stream(stream)))
+    return out
+
+
 def _run(fn, Q, K, V, extra, causal, out, stream):
     host = Q.device.type == "cpu"
     if host:
@@ -234,7 +254,11 @@ def _run(fn, Q, K, V, extra, causal, out, stream):
 
 
 def alibi_attn(Q, K, V, bins: Bins, causal: bool, out=None, stream=None):
-    """plsh_alibi_attn: approximate ALiBi attention T~ (Methodology 3)."""
+    """plsh_alibi_attn: approximate ALiBi attention T~ (Methodology 3).  Host
+    tensors go through plsh_alibi_attn_host (complete once `stream` is
+    synchronised)."""
+    if Q.device.type == "cpu":
+        return alibi_attn_host(Q, K, V, bins, causal, out, stream)
     return _run(load().plsh_alibi_attn, Q, K, V, bins.handle, causal, out, stream)
 
 

@@ -236,12 +236,12 @@ plsh_status check_qkvo(const plsh_tensor* Q, const plsh_tensor* K, const plsh_te
 // have similar key envelopes); an odd group's last head pairs its own row
 // tiles.  Ordered by expected cost, largest first, so that the dynamic queue
 // balances like longest-processing-time scheduling.
-std::vector<int4> build_items(int B, int Hq, int Hkv, int QT, bool exact,
+std::vector<int4> build_items(int B, int Hq, int Hkv, int qt0, int qt1, bool exact,
                               const std::vector<double>& sigma) {
   const int G = Hq / Hkv;
   std::vector<int4> items;
   std::vector<double> cost;
-  items.reserve((size_t)B * Hq * QT / 2 + B * Hkv);
+  items.reserve((size_t)B * Hq * (qt1 - qt0) / 2 + B * Hkv);
   for (int b = 0; b < B; ++b) {
     for (int kvh = 0; kvh < Hkv; ++kvh) {
       std::vector<int> heads(G);
@@ -251,15 +251,15 @@ std::vector<int4> build_items(int B, int Hq, int Hkv, int QT, bool exact,
                          [&](int x, int y) { return sigma[x] > sigma[y]; });
       for (int pr = 0; pr + 1 < G; pr += 2) {
         const int hA = heads[pr], hB = heads[pr + 1];
-        for (int qt = 0; qt < QT; ++qt) {
+        for (int qt = qt0; qt < qt1; ++qt) {
           items.push_back(make_int4(b, hA | (hB << 16), qt, qt));
           cost.push_back(exact ? (double)qt : std::max(sigma[hA], sigma[hB]) * 1e6 + qt);
         }
       }
       if (G % 2) {
         const int hL = heads[G - 1];
-        for (int qt = 0; qt < QT; qt += 2) {
-          const int qtB = qt + 1 < QT ? qt + 1 : -1;
+        for (int qt = qt0; qt < qt1; qt += 2) {
+          const int qtB = qt + 1 < qt1 ? qt + 1 : -1;
           items.push_back(make_int4(b, hL | (hL << 16), qt, qtB));
           cost.push_back(exact ? (double)std::max(qt, qtB) : sigma[hL] * 1e6 + qt);
         }
@@ -277,13 +277,15 @@ std::vector<int4> build_items(int B, int Hq, int Hkv, int QT, bool exact,
 
 // Device copy of the item table for this shape and head order (built and
 // uploaded on first use, then reused).
-plsh_status item_table(plsh::DeviceCtx* ctx, int B, int Hq, int Hkv, int QT, bool exact,
-                       const std::vector<double>& sigma, cudaStream_t st,
+plsh_status item_table(plsh::DeviceCtx* ctx, int B, int Hq, int Hkv, int qt0, int qt1,
+                       bool exact, const std::vector<double>& sigma, cudaStream_t st,
                        const int4** out, int* count) {
-  // the table depends on the shape and, for the approximate kernel, on the
-  // order of sigma inside each KV group and across heads
+  // the table depends on the shape, the range of query tiles and, for the
+  // approximate kernel, on the order of sigma inside each KV group and across
+  // heads
   std::string key = std::to_string(exact) + ":" + std::to_string(B) + ":" + std::to_string(Hq) +
-                    ":" + std::to_string(Hkv) + ":" + std::to_string(QT);
+                    ":" + std::to_string(Hkv) + ":" + std::to_string(qt0) + "-" +
+                    std::to_string(qt1);
   if (!exact) {
     std::vector<int> rank(Hq);
     std::iota(rank.begin(), rank.end(), 0);
@@ -304,7 +306,7 @@ plsh_status item_table(plsh::DeviceCtx* ctx, int B, int Hq, int Hkv, int QT, boo
       ctx->tables.erase(victim);
     }
     plsh::ItemTable t;
-    t.host = build_items(B, Hq, Hkv, QT, exact, sigma);
+    t.host = build_items(B, Hq, Hkv, qt0, qt1, exact, sigma);
     plsh_status s = dev_alloc((void**)&t.dev, sizeof(int4) * t.host.size(), "item table");
     if (s != PLSH_OK) return s;
     cudaError_t e = cudaMemcpyAsync(t.dev, t.host.data(), sizeof(int4) * t.host.size(),
@@ -333,7 +335,7 @@ Path path_override() {
 
 plsh_status run_attention(const plsh_tensor* Q, const plsh_tensor* K, const plsh_tensor* V,
                           plsh_tensor* O, int causal, const plsh_bins* bins,
-                          const float* slopes, cudaStream_t st) {
+                          const float* slopes, cudaStream_t st, int qt0 = 0, int qt1 = -1) {
   plsh::DeviceCtx* ctx = nullptr;
   plsh_status s0 = current_ctx(&ctx);
   if (s0 != PLSH_OK) return s0;
@@ -371,7 +373,7 @@ plsh_status run_attention(const plsh_tensor* Q, const plsh_tensor* K, const plsh
                                       "its shared-memory budget");
   if (path == Path::Tc) {
     const int QT = (int)((Q->n + 127) / 128);
-    plsh_status s1 = item_table(ctx, a.B, a.Hq, a.Hkv, QT, a.exact != 0,
+    plsh_status s1 = item_table(ctx, a.B, a.Hq, a.Hkv, qt0, qt1 < 0 ? QT : qt1, a.exact != 0,
                                 bins ? bins->sigma_host : std::vector<double>(), st,
                                 &a.items, &a.num_items);
     if (s1 != PLSH_OK) return s1;
@@ -575,6 +577,104 @@ plsh_status plsh_alibi_attn(const plsh_tensor* Q, const plsh_tensor* K, const pl
   if (bins->H != Q->H) return fail(PLSH_ERR_INVALID, "bins were drawn for another number of heads");
   if ((st = check_bins_device(bins)) != PLSH_OK) return st;
   return run_attention(Q, K, V, O, causal, bins, nullptr, (cudaStream_t)stream);
+}
+
+plsh_status plsh_alibi_attn_host(const plsh_tensor* Q, const plsh_tensor* K,
+                                 const plsh_tensor* V, const plsh_bins* bins, int32_t causal,
+                                 plsh_tensor* O, void* stream) {
+  plsh_status st = check_qkvo(Q, K, V, O);
+  if (st != PLSH_OK) return st;
+  if (bins == nullptr) return fail(PLSH_ERR_INVALID, "bins is NULL");
+  if (bins->n != Q->n) return fail(PLSH_ERR_INVALID, "bins were drawn for another n");
+  if (bins->H != Q->H) return fail(PLSH_ERR_INVALID, "bins were drawn for another number of heads");
+  if ((st = check_bins_device(bins)) != PLSH_OK) return st;
+  plsh::DeviceCtx* ctx = nullptr;
+  if ((st = current_ctx(&ctx)) != PLSH_OK) return st;
+  cudaStream_t cs = (cudaStream_t)stream;
+  const size_t esz = Q->dtype == PLSH_BF16 ? 2 : 4;
+  const int64_t n = Q->n, d = Q->d;
+  const size_t row = (size_t)d * esz;                       // bytes of one token row
+  const size_t bytes[4] = {(size_t)(Q->B * Q->H * n) * row, (size_t)(K->B * K->H * n) * row,
+                           (size_t)(V->B * V->H * n) * row, (size_t)(O->B * O->H * n) * row};
+  {
+    std::lock_guard<std::mutex> lk(g_ctx_mu);
+    if (ctx->h2d == nullptr) {
+      PLSH_TRY_CUDA(cudaStreamCreateWithFlags(&ctx->h2d, cudaStreamNonBlocking), "copy stream");
+      PLSH_TRY_CUDA(cudaStreamCreateWithFlags(&ctx->d2h, cudaStreamNonBlocking), "copy stream");
+      for (cudaEvent_t& e : ctx->ev)
+        PLSH_TRY_CUDA(cudaEventCreateWithFlags(&e, cudaEventDisableTiming), "event");
+    }
+    for (int k = 0; k < 4; ++k) {
+      if (ctx->stage_bytes[k] >= bytes[k]) continue;
+      // grow (the old buffer may still be in use by earlier calls)
+      PLSH_TRY_CUDA(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
+      cudaFree(ctx->stage[k]);
+      ctx->stage[k] = nullptr;
+      ctx->stage_bytes[k] = 0;
+      if ((st = dev_alloc(&ctx->stage[k], bytes[k], "host staging")) != PLSH_OK) return st;
+      ctx->stage_bytes[k] = bytes[k];
+    }
+  }
+  plsh_tensor dQ = *Q, dK = *K, dV = *V, dO = *O;
+  dQ.data = ctx->stage[0];
+  dK.data = ctx->stage[1];
+  dV.data = ctx->stage[2];
+  dO.data = ctx->stage[3];
+  // query rows in up to kMaxHostChunks chunks on the tensor-core path (one
+  // otherwise): the copies of chunk c + 1 in and chunk c - 1 out overlap the
+  // kernel on chunk c; without the causal mask every chunk needs all keys
+  const int QT = (int)((n + 127) / 128);
+  const bool tc = Q->dtype == PLSH_BF16 && Q->d == 128 && path_override() != Path::Simt &&
+                  plsh::attn_tc_smem_bytes(bins->s, causal ? 1 : 0, 0) <= 232448;
+  const int nchunk = tc ? std::min(plsh::kMaxHostChunks, QT) : 1;
+  const int tpc = (QT + nchunk - 1) / nchunk;
+  const bool kv_chunked = causal && nchunk > 1;
+  cudaEvent_t ev_start = ctx->ev[0], ev_done = ctx->ev[1];
+  // the staging buffers are free once everything queued on the stream is
+  PLSH_TRY_CUDA(cudaEventRecord(ev_start, cs), "event");
+  PLSH_TRY_CUDA(cudaStreamWaitEvent(ctx->h2d, ev_start, 0), "stream wait");
+  PLSH_TRY_CUDA(cudaStreamWaitEvent(ctx->d2h, ev_start, 0), "stream wait");
+  auto rows_copy = [&](void* dst, const void* src, int64_t heads, int64_t r0, int64_t r1,
+                       cudaMemcpyKind kind, cudaStream_t s2) -> cudaError_t {
+    // rows [r0, r1) of every (b, h): one strided copy
+    const size_t pitch = (size_t)n * row;
+    return cudaMemcpy2DAsync(static_cast<char*>(dst) + r0 * row, pitch,
+                             static_cast<const char*>(src) + r0 * row, pitch,
+                             (size_t)(r1 - r0) * row, (size_t)heads, kind, s2);
+  };
+  if (!kv_chunked) {
+    PLSH_TRY_CUDA(cudaMemcpyAsync(dK.data, K->data, bytes[1], cudaMemcpyHostToDevice, ctx->h2d),
+                  "copy K");
+    PLSH_TRY_CUDA(cudaMemcpyAsync(dV.data, V->data, bytes[2], cudaMemcpyHostToDevice, ctx->h2d),
+                  "copy V");
+  }
+  for (int c = 0; c < nchunk; ++c) {
+    const int qt0 = c * tpc, qt1 = std::min(QT, (c + 1) * tpc);
+    if (qt0 >= qt1) break;
+    const int64_t r0 = (int64_t)qt0 * 128, r1 = std::min(n, (int64_t)qt1 * 128);
+    cudaEvent_t ev_in = ctx->ev[2 + 2 * c], ev_out = ctx->ev[3 + 2 * c];
+    PLSH_TRY_CUDA(rows_copy(dQ.data, Q->data, Q->B * Q->H, r0, r1, cudaMemcpyHostToDevice,
+                            ctx->h2d), "copy Q rows");
+    if (kv_chunked) {
+      PLSH_TRY_CUDA(rows_copy(dK.data, K->data, K->B * K->H, r0, r1, cudaMemcpyHostToDevice,
+                              ctx->h2d), "copy K rows");
+      PLSH_TRY_CUDA(rows_copy(dV.data, V->data, V->B * V->H, r0, r1, cudaMemcpyHostToDevice,
+                              ctx->h2d), "copy V rows");
+    }
+    PLSH_TRY_CUDA(cudaEventRecord(ev_in, ctx->h2d), "event");
+    PLSH_TRY_CUDA(cudaStreamWaitEvent(cs, ev_in, 0), "stream wait");
+    if ((st = run_attention(&dQ, &dK, &dV, &dO, causal, bins, nullptr, cs,
+                            tc ? qt0 : 0, tc ? qt1 : -1)) != PLSH_OK)
+      return st;
+    PLSH_TRY_CUDA(cudaEventRecord(ev_out, cs), "event");
+    PLSH_TRY_CUDA(cudaStreamWaitEvent(ctx->d2h, ev_out, 0), "stream wait");
+    PLSH_TRY_CUDA(rows_copy(O->data, dO.data, O->B * O->H, r0, r1, cudaMemcpyDeviceToHost,
+                            ctx->d2h), "copy O rows");
+  }
+  // the caller's stream continues once O is on the host
+  PLSH_TRY_CUDA(cudaEventRecord(ev_done, ctx->d2h), "event");
+  PLSH_TRY_CUDA(cudaStreamWaitEvent(cs, ev_done, 0), "stream wait");
+  return PLSH_OK;
 }
 
 plsh_status plsh_alibi_exact(const plsh_tensor* Q, const plsh_tensor* K, const plsh_tensor* V,

@@ -35,6 +35,7 @@ struct ItemTable {
 };
 
 // Per-device library state.
+constexpr int kMaxHostChunks = 4;    // query-row chunks of the host-buffer entry point
 struct DeviceCtx {
   int device = -1;
   int num_sms = 0;
@@ -44,6 +45,12 @@ struct DeviceCtx {
   uint64_t wait_ns = kDefaultWaitNs;
   std::map<std::string, ItemTable> tables;
   uint64_t table_clock = 0;
+  // staging of the host-buffer entry point: device copies of Q, K, V, O,
+  // one stream per copy direction and the events that chain the chunks
+  void* stage[4] = {nullptr, nullptr, nullptr, nullptr};
+  size_t stage_bytes[4] = {0, 0, 0, 0};
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t ev[2 + 2 * kMaxHostChunks] = {};
 };
 constexpr size_t kMaxTables = 16;
 constexpr int kQueueSlots = 1024;
