@@ -13,34 +13,36 @@
 // contains i, so the keys with c_ij > 0 form one interval [lo_min(i), i]
 // (or [lo_min, hi_max) without the causal mask), and inside it c_i(j) is a
 // step function of j that rises at the bin starts lo_t(i) (and falls at the
-// bin ends hi_t(i) when not causal).  The row's thread keeps those starts
-// sorted in shared memory and walks them while it sweeps the key tiles: a
-// 32-key chunk with no step takes log2(c) into the exponent's FMA offset, a
-// chunk with steps adds one ramp per distinct step position.
+// bin ends hi_t(i) when not causal).  The row's thread holds those starts
+// in registers (s <= 16; counted per 32-key chunk) or sorted in shared
+// memory (walked by pointers); a chunk with no step takes log2(c) into the
+// exponent's offset, a chunk with steps multiplies by the running count.
 //
 // Exact ALiBi (the dense comparator) runs on the same pipeline with weight
 // e^{S_ij - |i-j|/sigma_h} over every key tile.
 //
-// One persistent CTA per SM, 10 warps, two 128-row query tiles A and B per
+// One persistent CTA per SM, 11 warps, two 128-row query tiles A and B per
 // work item (two heads of one KV group at the same rows, or two row tiles of
 // one head), sharing every K/V tile:
-//   warp 8      producer: pops items from a global queue in cost order,
+//   warp 10     scheduler: pops items from a global queue (cost order),
 //               stages the rows' bin records in shared memory, finds the key
-//               envelope, TMA-loads Q_A, Q_B and the K/V tiles (a ring of
-//               three 32 KB slots) from the diagonal tile down;
-//   warp 9      one thread issues tcgen05.mma in the order
-//               S_A(g) S_B(g) PV_A(g) S_A(g+1) PV_B(g) S_B(g+1) ...
-//               so that while one warpgroup turns its scores into weights the
-//               tensor core works for the other (tcgen05 MMAs of one thread
-//               execute in issue order: the commit that follows S_X(g) also
-//               proves PV_X(g-1) has landed);
+//               envelope and publishes the item in a three-deep ring;
+//   warp 8      producer: TMA-loads the item's first K tile, then Q_A and
+//               Q_B, then the other K/V tiles from the diagonal tile down
+//               (a ring of three 32 KB slots);
+//   warp 9      one thread issues tcgen05.mma in one stream across items,
+//               PV_A(g-1) S_A(g) PV_B(g-1) S_B(g) ..., so that while one
+//               warpgroup turns its scores into weights the tensor core works
+//               for the other (tcgen05 MMAs of one thread execute in issue
+//               order: the commit that follows S_X(g) also proves PV_X(g-1)
+//               has landed);
 //   warps 0-3   softmax of tile A, warps 4-7 softmax of tile B: one thread
 //               per row, tcgen05.ld of the score row, running max over the
 //               valid keys, lazy rescale of O in TMEM (only when the max grows
 //               by more than 2^8), P = c 2^(x - m) split into two bf16 terms
 //               P_hi + P_lo (truncated head, rounded remainder) written back
-//               over the consumed score columns,
-//               fp32 row sums, and the O / l epilogue.
+//               over the consumed score columns, fp32 row sums, and the O / l
+//               epilogue (through shared memory into whole-line stores).
 //   O += P_hi V + P_lo V runs as two tensor-core products with A read from
 //   TMEM: a single bf16 P carries a 2^-9 relative error per weight, which
 //   shows in rows whose few keys cancel; the pair carries about 2^-16.
