@@ -74,7 +74,8 @@ constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kSchedWarp = 10;
 constexpr int kRing = 3;                         // work items in flight
-constexpr int kMaxSlots = 4;                     // K/V tile ring (3 or 4 slots)
+constexpr int kSlots = 3;                        // K/V tile ring depth
+constexpr int kMaxSlots = 4;                     // barriers reserved for the ring
 constexpr uint32_t kTileBytes = BM * HD * 2;     // 32 KB bf16 tile
 constexpr uint32_t kHalfBytes = kTileBytes / 2;  // one 64-column TMA box
 constexpr uint32_t OFF_Q = 0;                          // Q_A, Q_B
@@ -109,7 +110,6 @@ struct TcParams {
   AttnArgs a;
   float slope_log2[512];   // exact mode: log2(e) / sigma_h
   int QT;                  // query tiles per (b, h)
-  int slots;               // K/V ring depth
   int out_smem;            // 1: the epilogue transposes O through shared memory
 };
 
@@ -245,8 +245,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
   const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (sbase - raw_u32);
   const int s = a.s;
-  const int nslots = p.slots;
-  const uint32_t off_out = OFF_KV + (uint32_t)nslots * kTileBytes;   // 8 warps x 4 KB
+  constexpr uint32_t nslots = kSlots;
+  const uint32_t off_out = OFF_KV + nslots * kTileBytes;   // 8 warps x 4 KB
   const uint32_t off_bp = off_out + (p.out_smem ? kOutBytes : 0u);
   int* bp = reinterpret_cast<int*>(smem + off_bp);
   uint4* stage = reinterpret_cast<uint4*>(smem + off_bp + bp_bytes(s, EXACT, CAUSAL, SREG));
@@ -415,8 +415,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         const int kvp = it.b * Hkv + it.hA / (Hq / Hkv);
         for (int kt = it.kt_hi - 1; ok && kt >= it.kt_lo; --kt) {
           for (int kv = 0; kv < 2 && ok; ++kv, ++ld) {
-            const int sl = ld % nslots;
-            const uint32_t u = (uint32_t)(ld / nslots);
+            const uint32_t sl = (uint32_t)ld % nslots;
+            const uint32_t u = (uint32_t)ld / nslots;
             ok = mbar_wait(bar(B_KVEMPTY + sl), (u & 1u) ^ 1u, abort, lim);
             if (!ok) break;
             const uint32_t dst = sbase + OFF_KV + sl * kTileBytes;
@@ -453,7 +453,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         mbar_wait(bar(B_QFULL + 0), (uint32_t)(q_issued - 1) & 1u, nullptr, lim);
         mbar_wait(bar(B_QFULL + 1), (uint32_t)(q_issued - 1) & 1u, nullptr, lim);
       }
-      for (int sl = 0; sl < nslots; ++sl)
+      for (uint32_t sl = 0; sl < nslots; ++sl)
         if (kv_issued[sl])
           mbar_wait(bar(B_KVFULL + sl), (uint32_t)(kv_issued[sl] - 1) & 1u, nullptr, lim);
     }
@@ -467,28 +467,34 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       int ld = 0;        // K/V loads consumed so far (same numbering as producer)
       int gt = 0;        // tiles processed so far (both tiles advance together)
       auto wait_slot = [&](int l) -> bool {
-        return mbar_wait(bar(B_KVFULL + l % nslots), (uint32_t)(l / nslots) & 1u, abort, lim);
+        return mbar_wait(bar(B_KVFULL + (uint32_t)l % nslots), ((uint32_t)l / nslots) & 1u, abort,
+                        lim);
       };
+      // descriptors of the tiles' first 16-column slices; a slice further
+      // on adds its byte offset / 16 to the start-address field
+      const uint64_t dq0 = desc_sw128(sbase + OFF_Q, 16, 1024);
+      const uint64_t dk0 = desc_sw128(sbase + OFF_KV, 16, 1024);
+      const uint64_t dv0 = desc_sw128(sbase + OFF_KV, kHalfBytes, 1024);
       auto issue_s = [&](int tile, int lk) {
-        const uint32_t qbase = sbase + OFF_Q + tile * kTileBytes;
-        const uint32_t kbase = sbase + OFF_KV + (lk % nslots) * kTileBytes;
+        const uint64_t qd = desc_add(dq0, tile * (kTileBytes >> 4));
+        const uint64_t kd = desc_add(dk0, ((uint32_t)lk % nslots) * (kTileBytes >> 4));
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t koff = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-          mma_bf16_ss(tmem + tile * BN, desc_sw128(qbase + koff, 16, 1024),
-                      desc_sw128(kbase + koff, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+          const uint32_t koff = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+          mma_bf16_ss(tmem + tile * BN, desc_add(qd, koff), desc_add(kd, koff), idesc_qk,
+                      kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(B_SFULL + tile));
       };
       auto issue_pv = [&](int tile, int lv, bool first) {
-        const uint32_t vbase = sbase + OFF_KV + (lv % nslots) * kTileBytes;
+        const uint64_t vd = desc_add(dv0, ((uint32_t)lv % nslots) * (kTileBytes >> 4));
         // keys 16kk..16kk+15 sit in chunk kk/2: P_hi in its first 16
         // columns, P_lo in the next 16, 8 packed columns per 16 keys
         const uint32_t pcol = tmem + tile * BN;
         const uint32_t ocol = tmem + kColO + tile * HD;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t bd = desc_sw128(vbase + kk * 2048, kHalfBytes, 1024);
+          const uint64_t bd = desc_add(vd, kk * (2048 >> 4));
           const uint32_t ac = pcol + (kk >> 1) * 32 + (kk & 1) * 8;
           mma_bf16_ts(ocol, ac, bd, idesc_pv, (first && kk == 0) ? 0u : 1u);
           mma_bf16_ts(ocol, ac + 16, bd, idesc_pv, 1u);
@@ -528,7 +534,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
           if (!ok) break;
           tc_fence_after();
           issue_pv(1, prev_lv, prev_first);
-          mma_commit(bar(B_KVEMPTY + prev_lv % nslots));
+          mma_commit(bar(B_KVEMPTY + (uint32_t)prev_lv % nslots));
           if (prev_last) {
             mma_commit(bar(B_ODONE + 1));
             mbar_arrive(bar(B_IEMPTY + prev_slot));
@@ -540,7 +546,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         }
         tc_fence_after();
         issue_s(1, lk);
-        mma_commit(bar(B_KVEMPTY + lk % nslots));
+        mma_commit(bar(B_KVEMPTY + (uint32_t)lk % nslots));
         if (jj == T - 1) mma_commit(bar(B_QEMPTY + 1));
         have_prev = true;
         prev_lv = lk + 1;
@@ -571,7 +577,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         if (ok) {
           tc_fence_after();
           issue_pv(1, prev_lv, prev_first);
-          mma_commit(bar(B_KVEMPTY + prev_lv % nslots));
+          mma_commit(bar(B_KVEMPTY + (uint32_t)prev_lv % nslots));
           mma_commit(bar(B_ODONE + 1));
           mbar_arrive(bar(B_IEMPTY + prev_slot));
         }
@@ -1192,9 +1198,8 @@ size_t smem_for(int slots, bool out, int s, int causal, int exact) {
          sizeof(Ctl);
 }
 
-// Three K/V slots; the output staging buffer when the per-row bin lists
-// leave room for it (else the epilogue stores its rows directly).
-constexpr int kSlots = 3;
+// The output staging buffer when the per-row bin lists leave room for it
+// (else the epilogue stores its rows directly).
 bool out_staged(int s, int causal, int exact) {
   return smem_for(kSlots, true, s, causal, exact) <= kSmemLimit;
 }
@@ -1216,7 +1221,6 @@ cudaError_t launch_attn_tc(const AttnArgs& a, const float* slopes_host,
   for (int h = 0; h < 512; ++h)
     p.slope_log2[h] = (slopes_host && h < a.Hq) ? slopes_host[h] : 0.f;
   p.QT = (a.n + BM - 1) / BM;
-  p.slots = kSlots;
   p.out_smem = out_staged(a.s, a.causal, a.exact) ? 1 : 0;
   const int grid = a.num_items < num_sms ? a.num_items : num_sms;
   const size_t smem = attn_tc_smem_bytes(a.s, a.causal, a.exact);

@@ -232,6 +232,13 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo,
   return d;
 }
 
+// The descriptor of the operand `k` x 16 bytes further on: the start-address
+// field (bits 0-13) holds the shared-memory address / 16, and every address
+// below 256 KB fits it, so the sum never carries into the next field.
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t k) {
+  return (d & 0xffffffff00000000ull) | (uint64_t)((uint32_t)d + k);
+}
+
 // Instruction descriptor of kind::f16: fp32 accumulator (bits 4-5 = 1), bf16
 // A and B (bits 7-9 = 1, 10-12 = 1), A/B major in bits 15/16 (0 = K-major,
 // 1 = MN-major), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
