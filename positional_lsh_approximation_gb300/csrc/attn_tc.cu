@@ -83,6 +83,7 @@ constexpr uint32_t OFF_KV = OFF_Q + 2 * kTileBytes;    // ring of `slots` tiles
 constexpr uint32_t kTmemCols = 512;   // S_A | S_B | O_A | O_B; P over S
 constexpr uint32_t kColO = 256;
 constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (factor 256)
+constexpr float kGrowLog2 = 24.0f;    // largest weight 2^24 c before a mid-tile rescale
 constexpr unsigned FULL = 0xffffffffu;
 constexpr int kWordsPerTile = BM / 32;
 constexpr uint32_t kOutBytes = 8 * 32 * 64 * 2;   // O transpose: 32 rows x 64 bf16 per warp
@@ -775,73 +776,85 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         if (!ok) break;
         tc_fence_after();
 
-        // pass 1: running max (log2 units) over the keys that take part
-        float mx0 = -INFINITY, mx1 = -INFINITY;
+        // exact ALiBi: after a row's first tile the weights are taken against
+        // the running max as it stands and pass 2 watches for growth; the
+        // first tile (or a warp with a row that has no max yet) finds the
+        // tile's max first.  (The approximation keeps both passes: its masked
+        // chunks skip most of pass 1 already, and the growth check costs it
+        // registers.)
+        const bool one_pass =
+            EXACT && jj > 0 && !__any_sync(FULL, row_ok && m_ref == -INFINITY);
+        float m_use = m_ref, alpha = 1.f;
+        bool resc = false;
+        if (!one_pass) {
+          // pass 1: running max (log2 units) over the keys that take part
+          float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-        for (int q2 = 0; q2 < 2; ++q2) {
-          uint32_t vmh[2];
-          uint32_t ra[32], rb2[32];
-          if (EXACT) {
-            tmem_ld32(s_col + q2 * 64, ra);
-            tmem_ld32(s_col + q2 * 64 + 32, rb2);
-          }
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            const int jc = jt + q2 * 64 + half * 32;
-            vmh[half] = EXACT ? key_mask(-1, CAUSAL ? i - jc : n - 1 - jc, row_ok)
-                              : key_mask(vlo - jc, vhi - jc, row_ok);
-          }
-          if (!EXACT) {
-            // 64 keys that no row of this warp takes: nothing to read
-            if (!__any_sync(FULL, (vmh[0] | vmh[1]) != 0u)) continue;
-            tmem_ld32(s_col + q2 * 64, ra);
-            tmem_ld32(s_col + q2 * 64 + 32, rb2);
-          }
-          tmem_wait_ld();
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            const uint32_t* rr = half ? rb2 : ra;
-            const int jc = jt + q2 * 64 + half * 32;
-            float xv[32];
-            const uint32_t vm = vmh[half];
+          for (int q2 = 0; q2 < 2; ++q2) {
+            uint32_t vmh[2];
+            uint32_t ra[32], rb2[32];
             if (EXACT) {
-              const float d0 = (float)(i - jc);
+              tmem_ld32(s_col + q2 * 64, ra);
+              tmem_ld32(s_col + q2 * 64 + 32, rb2);
+            }
 #pragma unroll
-              for (int e = 0; e < 32; e += 2) {
-                if (CAUSAL) {
-                  const uint64_t b2 = f2_add(eslope[e >> 1], f2_pack(-d0 * slope, -d0 * slope));
-                  f2_unpack(f2_fma(f2_pack(__uint_as_float(rr[e]), __uint_as_float(rr[e + 1])),
-                                   scale2, b2), xv[e], xv[e + 1]);
-                } else {
-                  xv[e] = fmaf(__uint_as_float(rr[e]), scale_log2, -fabsf(d0 - (float)e) * slope);
-                  xv[e + 1] = fmaf(__uint_as_float(rr[e + 1]), scale_log2,
-                                   -fabsf(d0 - (float)(e + 1)) * slope);
+            for (int half = 0; half < 2; ++half) {
+              const int jc = jt + q2 * 64 + half * 32;
+              vmh[half] = EXACT ? key_mask(-1, CAUSAL ? i - jc : n - 1 - jc, row_ok)
+                                : key_mask(vlo - jc, vhi - jc, row_ok);
+            }
+            if (!EXACT) {
+              // 64 keys that no row of this warp takes: nothing to read
+              if (!__any_sync(FULL, (vmh[0] | vmh[1]) != 0u)) continue;
+              tmem_ld32(s_col + q2 * 64, ra);
+              tmem_ld32(s_col + q2 * 64 + 32, rb2);
+            }
+            tmem_wait_ld();
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              const uint32_t* rr = half ? rb2 : ra;
+              const int jc = jt + q2 * 64 + half * 32;
+              float xv[32];
+              const uint32_t vm = vmh[half];
+              if (EXACT) {
+                const float d0 = (float)(i - jc);
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                  if (CAUSAL) {
+                    const uint64_t b2 = f2_add(eslope[e >> 1], f2_pack(-d0 * slope, -d0 * slope));
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(rr[e]), __uint_as_float(rr[e + 1])),
+                                     scale2, b2), xv[e], xv[e + 1]);
+                  } else {
+                    xv[e] = fmaf(__uint_as_float(rr[e]), scale_log2, -fabsf(d0 - (float)e) * slope);
+                    xv[e + 1] = fmaf(__uint_as_float(rr[e + 1]), scale_log2,
+                                     -fabsf(d0 - (float)(e + 1)) * slope);
+                  }
                 }
+              } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) xv[e] = __uint_as_float(rr[e]);
               }
-            } else {
+              if (__any_sync(FULL, vm != 0xffffffffu)) {
 #pragma unroll
-              for (int e = 0; e < 32; ++e) xv[e] = __uint_as_float(rr[e]);
-            }
-            if (__any_sync(FULL, vm != 0xffffffffu)) {
+                for (int e = 0; e < 32; ++e)
+                  if (!(vm & (1u << e))) xv[e] = -INFINITY;
+              }
 #pragma unroll
-              for (int e = 0; e < 32; ++e)
-                if (!(vm & (1u << e))) xv[e] = -INFINITY;
-            }
-#pragma unroll
-            for (int e = 0; e < 32; e += 4) {
-              mx0 = max3(mx0, xv[e], xv[e + 1]);
-              mx1 = max3(mx1, xv[e + 2], xv[e + 3]);
+              for (int e = 0; e < 32; e += 4) {
+                mx0 = max3(mx0, xv[e], xv[e + 1]);
+                mx1 = max3(mx1, xv[e + 2], xv[e + 3]);
+              }
             }
           }
+          float mt = fmaxf(mx0, mx1);
+          if (!EXACT) mt *= scale_log2;
+          if (!row_ok) mt = -INFINITY;
+          const float m_new = fmaxf(m_ref, mt);
+          resc = m_new > m_ref + kRescaleLog2;
+          m_use = resc ? m_new : m_ref;
+          alpha = resc ? ex2(m_ref - m_new) : 1.f;
         }
-        float mt = fmaxf(mx0, mx1);
-        if (!EXACT) mt *= scale_log2;
-        if (!row_ok) mt = -INFINITY;
-        const float m_new = fmaxf(m_ref, mt);
-        const bool resc = m_new > m_ref + kRescaleLog2;
-        const float m_use = resc ? m_new : m_ref;
-        const float alpha = resc ? ex2(m_ref - m_new) : 1.f;
-        const float mu = (m_use == -INFINITY || !row_ok) ? 0.f : m_use;
+        float mu = (m_use == -INFINITY || !row_ok) ? 0.f : m_use;
 
         // a grown max rescales O; the commit behind S(g) proves P V(g-1) landed
         if (jj > 0 && __any_sync(FULL, resc)) {
@@ -992,9 +1005,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
           uint32_t hi[16], lo[16];
           {
             const bool all_flat = EXACT || __all_sync(FULL, flat);
+            const float lgb = (!EXACT && all_flat) ? lg2((float)max(base, 1)) : 0.f;
             float off;
             if (EXACT) off = -(float)(i - jc) * slope - mu;
-            else off = (all_flat ? lg2((float)max(base, 1)) : 0.f) - mu;
+            else off = lgb - mu;
             float pv[32];
 #pragma unroll
             for (int e = 0; e < 32; e += 2) {
@@ -1017,6 +1031,49 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
 #pragma unroll
               for (int e = 0; e < 32; ++e)
                 if (!(vm & (1u << e))) pv[e] = -INFINITY;
+            }
+            if (one_pass) {
+              // the chunk's largest exponent: far above the running max (a
+              // jump of the scores), O, l and the chunks of this tile written
+              // so far are scaled down to the new max first (by a power of
+              // two: exact in fp32 and in both bf16 terms)
+              float c0 = -INFINITY, c1 = -INFINITY;
+#pragma unroll
+              for (int e = 0; e < 32; e += 4) {
+                c0 = max3(c0, pv[e], pv[e + 1]);
+                c1 = max3(c1, pv[e + 2], pv[e + 3]);
+              }
+              const float cm = fmaxf(c0, c1);
+              if (__any_sync(FULL, cm > kGrowLog2)) {
+                const float d = cm > kGrowLog2 ? cm - lgb : 0.f;
+                const float f = ex2(-d);
+                mu += d;
+                if (row_ok) m_use = mu;
+#pragma unroll
+                for (int e = 0; e < 32; ++e) pv[e] -= d;
+                l *= f;
+                lsum2 = f2_mul(lsum2, f2_pack(f, f));
+#pragma unroll 1
+                for (int q3 = 0; q3 < 4; ++q3) {
+                  uint32_t o[32];
+                  tmem_ld32(o_col + q3 * 32, o);
+                  tmem_wait_ld();
+#pragma unroll
+                  for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+                  tmem_st32(o_col + q3 * 32, o);
+                }
+#pragma unroll 1
+                for (int q3 = 3; q3 > q; --q3) {
+                  uint32_t w[32];
+                  tmem_ld32(s_col + q3 * 32, w);
+                  tmem_wait_ld();
+#pragma unroll
+                  for (int e = 0; e < 32; ++e)
+                    w[e] = pack_bf16(__uint_as_float(w[e] << 16) * f,
+                                     __uint_as_float(w[e] & 0xffff0000u) * f);
+                  tmem_st32(s_col + q3 * 32, w);
+                }
+              }
             }
 #pragma unroll
             for (int e = 0; e < 32; ++e) pv[e] = ex2(pv[e]);

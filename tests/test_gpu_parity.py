@@ -177,6 +177,48 @@ def test_special_cases_single_bin_and_singletons():
     np.testing.assert_array_equal(got[0, 1], V[0, 0])
 
 
+@pytest.mark.parametrize("causal", [True, False], ids=["causal", "noncausal"])
+def test_score_jump_in_a_later_key_tile(causal):
+    """Keys 0..127 scaled by 16 (exact in bf16): every row that reaches them
+    meets scores far above the running max it carried from the key tiles
+    nearer its diagonal, so the kernel rescales O, l and the weights already
+    written in the middle of a tile; all rows against the oracle."""
+    n, s = 700, 6
+    w = Workload("jump", 1, 2, 1, n, 128, "bf16", causal, s, (60.0, 400.0), qkv_seed=31)
+    Q, K, V = make_qkv(w)
+    K = K.copy()
+    K[:, :, :128, :] *= 16.0
+    sigma = w.sigmas()
+    bins = plsh.sample_bins(n, sigma, s, seed=8)
+    off, st = oracle.sample_bins(n, sigma, s, seed=8)
+    rows = oracle.all_rows(1, 2, n)
+    O = run_approx(w, Q, K, V, bins)
+    ref = oracle.plsh_attn_rows(Q, K, V, off, st, s, causal, rows)
+    assert_close(gather_rows(O, rows), ref, "bf16", "score jump, approx")
+    E = plsh.alibi_exact(to_dev(Q, "bf16"), to_dev(K, "bf16"), to_dev(V, "bf16"), sigma, causal)
+    plsh.stream_status()
+    ref = oracle.alibi_exact_rows(Q, K, V, sigma, causal, rows)
+    assert_close(gather_rows(E, rows), ref, "bf16", "score jump, exact")
+    bins.free()
+
+
+def test_peaky_rows_all_rows():
+    """5 % of token rows with Q and K scaled by 8 (the Qwen-shaped inputs),
+    small enough for every row against the oracle, both masks."""
+    for causal in (True, False):
+        w = Workload("peaky", 1, 4, 2, 900, 128, "bf16", causal, 10, (2.0, 9.0, 50.0, 250.0),
+                     peaky_frac=0.05, qkv_seed=41)
+        Q, K, V = make_qkv(w)
+        sigma = w.sigmas()
+        bins = plsh.sample_bins(w.n, sigma, w.s, seed=2)
+        off, st = oracle.sample_bins(w.n, sigma, w.s, seed=2)
+        rows = oracle.all_rows(1, 4, w.n)
+        O = run_approx(w, Q, K, V, bins)
+        ref = oracle.plsh_attn_rows(Q, K, V, off, st, w.s, causal, rows)
+        assert_close(gather_rows(O, rows), ref, "bf16", f"peaky causal={causal}")
+        bins.free()
+
+
 def test_repeated_calls_reuse_queue_and_agree():
     w = WORKLOADS["mistral"].with_(n=2048)
     Q, K, V = make_qkv(w)
