@@ -350,9 +350,71 @@ def run_ours(args, rank, world):
         "approx_error_vs_exact": approx_err,
         "clocks": clocks.summary(),
     }
+    result["decode"] = measure_decode(w, bins, sigma, flush, stream)
     if rank == 0 and not args.no_cpu:
         result["cpu_baseline"] = cpu_baseline(w, Qn, Kn, Vn, offsets, starts, args.cpu_seconds)
     return result
+
+
+# ------------------------------------------------------------ decode step
+DECODE_BATCH = 64
+
+
+def measure_decode(w, bins, sigma, flush, stream, iters=20):
+    """One decode step (plsh_alibi_decode) for a batch of DECODE_BATCH
+    sequences whose caches hold the workload's n positions, the query at the
+    last one; same heads, hashes and scales as the workload.  Bound by HBM:
+    the algorithmic bytes are the K and V rows of each KV group's widest key
+    envelope (every query head of a group reads inside it) plus q and o."""
+    import torch
+    import positional_lsh_approximation_gb300 as plsh
+    if not w.causal:
+        return None
+    dev = stream.device
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    esz = 2 if w.dtype == "bf16" else 4
+    g = torch.Generator(device=dev)
+    g.manual_seed(4242)
+    Bd, pos = DECODE_BATCH, w.n - 1
+    K = torch.randn(Bd, w.Hkv, w.n, w.d, generator=g, device=dev).to(tdt)
+    V = torch.randn(Bd, w.Hkv, w.n, w.d, generator=g, device=dev).to(tdt)
+    q = torch.randn(Bd, w.Hq, 1, w.d, generator=g, device=dev).to(tdt)
+    o = torch.empty_like(q)
+    offsets, starts = bins.to_host()
+    env = []
+    for h in range(w.Hq):
+        lo = pos
+        for t in range(w.s):
+            st = starts[offsets[h * w.s + t]:offsets[h * w.s + t + 1]]
+            lo = min(lo, int(st[np.searchsorted(st, pos, side="right") - 1]))
+        env.append(pos - lo + 1)
+    per_group = w.Hq // w.Hkv
+    widest = [max(env[g0 * per_group:(g0 + 1) * per_group]) for g0 in range(w.Hkv)]
+    bytes_ = Bd * (sum(widest) * 2 * w.d * esz + 2 * w.Hq * w.d * esz)
+    for _ in range(3):
+        plsh.alibi_decode(q, K, V, bins, pos, out=o)
+    plsh.stream_status()
+    ms = []
+    for _ in range(iters):
+        # evict L2 by reading a buffer larger than it: a written flush would
+        # leave ~129 MB of dirty lines whose write-back lands in this short step
+        flush.sum()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        plsh.alibi_decode(q, K, V, bins, pos, out=o)
+        b.record(stream)
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    plsh.stream_status()
+    t = statistics.median(ms) / 1e3
+    pk = peaks()
+    return {"batch": Bd, "n_cache": w.n, "pos": pos, "tokens_per_s": Bd / t, "ms": t * 1e3,
+            "envelope_keys_mean": float(np.mean(env)), "bytes": bytes_,
+            "achieved_gbs": bytes_ / t / 1e9, "peak_gbs": pk["hbm_gbs"],
+            "hbm_frac": bytes_ / t / 1e9 / pk["hbm_gbs"], "peak_source": pk["source"],
+            "kernels": "decode_partial_kernel + decode_merge_kernel",
+            "l2": "evicted before each step (256 MiB read)"}
 
 
 # ---------------------------------------------------------- oracle on CPU

@@ -216,6 +216,29 @@ plsh_status plsh_alibi_exact(const plsh_tensor* Q, const plsh_tensor* K,
                              const plsh_tensor* V, const double* sigma_h,
                              int32_t causal, plsh_tensor* O, void* stream);
 
+/*
+ * plsh_alibi_decode -- one decode step of the approximation: row `pos` of T~
+ * (Methodology 3) with the causal mask, for a query given on its own against
+ * cached keys and values.  With J_t(pos) = [lo_t(pos), pos], lo_t(pos) the
+ * start of the bin of pos under hash t of head h,
+ *   o = sum_j c_j e^{S_j} v_j / sum_j c_j e^{S_j},  S_j = q . k_j / sqrt(d),
+ *   c_j = #{t : lo_t(pos) <= j},  j in [min_t lo_t(pos), pos]:
+ * the work is the row's key envelope, O(s b) keys, not pos.
+ *
+ *   q [B,Hq,1,d]: the query of position pos; o [B,Hq,1,d]: its output.
+ *   K, V [B,Hkv,n,d]: the cache; rows above pos are not read.
+ *   All the same dtype (PLSH_BF16 or PLSH_F32), d in {64, 128}, Hq % Hkv == 0,
+ *   B * Hq <= 65535, bins->n == n, bins->H == Hq, 0 <= pos < n.
+ * The key envelope is split into chunks of 512 keys whose partial results
+ * (max, row sum, unnormalised P V) are merged into o; the partials live in a
+ * device buffer the library keeps per device (B * Hq * (pos/512 + 1) *
+ * (d + 2) floats, grown on demand, which synchronises the device).
+ * Asynchronous on `stream`; errors in the arguments return before any launch.
+ */
+plsh_status plsh_alibi_decode(const plsh_tensor* q, const plsh_tensor* K,
+                              const plsh_tensor* V, const plsh_bins* bins, int64_t pos,
+                              plsh_tensor* o, void* stream);
+
 /* Synchronises `stream`, then reports CUDA errors and the library's device
  * error flag (PLSH_ERR_TIMEOUT when a bounded device wait ran out), clearing
  * the flag. */

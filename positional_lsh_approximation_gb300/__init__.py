@@ -22,7 +22,7 @@ from . import build as _build_mod
 
 __all__ = ["build", "load", "sample_bins", "bins_from_host", "Bins", "alibi_attn",
            "alibi_attn_noalloc", "alibi_attn_host",
-           "alibi_exact", "stream_status", "set_wait_limit_ns", "PlshError",
+           "alibi_exact", "alibi_decode", "stream_status", "set_wait_limit_ns", "PlshError",
            "library_path"]
 
 PLSH_OK, PLSH_ERR_INVALID, PLSH_ERR_CUDA, PLSH_ERR_NOMEM, PLSH_ERR_TIMEOUT, \
@@ -82,6 +82,7 @@ def load():
             "plsh_alibi_attn_noalloc": [TP, TP, TP, P, I32, TP, P],
             "plsh_alibi_attn_host": [TP, TP, TP, P, I32, TP, P],
             "plsh_alibi_exact": [TP, TP, TP, D, I32, TP, P],
+            "plsh_alibi_decode": [TP, TP, TP, P, I64, TP, P],
             "plsh_stream_status": [P],
             "plsh_set_wait_limit_ns": [U64],
         }
@@ -273,6 +274,19 @@ def alibi_exact(Q, K, V, sigma, causal: bool, out=None, stream=None):
     sig = _f64(sigma)
     return _run(load().plsh_alibi_exact, Q, K, V,
                 sig.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), causal, out, stream)
+
+
+def alibi_decode(q, K, V, bins: Bins, pos: int, out=None, stream=None):
+    """plsh_alibi_decode: one decode step, row `pos` of T~ (causal) for the
+    query q [B, Hq, 1, d] against the cache K, V [B, Hkv, n, d] (device
+    tensors)."""
+    if q.device.type == "cpu":
+        raise ValueError("alibi_decode: q, K, V must be device tensors")
+    o = torch.empty_like(q) if out is None else out
+    tq, tk, tv, to = _desc(q), _desc(K), _desc(V), _desc(o)
+    _check(load().plsh_alibi_decode(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv),
+                                    bins.handle, int(pos), ctypes.byref(to), _stream(stream)))
+    return o
 
 
 def stream_status(stream=None):

@@ -677,6 +677,70 @@ plsh_status plsh_alibi_attn_host(const plsh_tensor* Q, const plsh_tensor* K,
   return PLSH_OK;
 }
 
+plsh_status plsh_alibi_decode(const plsh_tensor* q, const plsh_tensor* K, const plsh_tensor* V,
+                              const plsh_bins* bins, int64_t pos, plsh_tensor* o, void* stream) {
+  plsh_status st;
+  if ((st = check_tensor(q, "q")) != PLSH_OK || (st = check_tensor(K, "K")) != PLSH_OK ||
+      (st = check_tensor(V, "V")) != PLSH_OK || (st = check_tensor(o, "o")) != PLSH_OK)
+    return st;
+  if (K->dtype != q->dtype || V->dtype != q->dtype || o->dtype != q->dtype)
+    return fail(PLSH_ERR_INVALID, "q, K, V and o must share one dtype");
+  if (q->d != 64 && q->d != 128) return fail(PLSH_ERR_INVALID, "head dim d must be 64 or 128");
+  if (q->n != 1) return fail(PLSH_ERR_INVALID, "q must be [B, Hq, 1, d]");
+  if (o->B != q->B || o->H != q->H || o->n != 1 || o->d != q->d)
+    return fail(PLSH_ERR_INVALID, "o must have q's shape");
+  if (K->B != q->B || K->d != q->d)
+    return fail(PLSH_ERR_INVALID, "K must be [B, Hkv, n, d] with q's B and d");
+  if (V->B != K->B || V->H != K->H || V->n != K->n || V->d != K->d)
+    return fail(PLSH_ERR_INVALID, "V must have K's shape");
+  if (q->H % K->H != 0) return fail(PLSH_ERR_INVALID, "Hq must be a multiple of Hkv");
+  if (K->n >= ((int64_t)1 << 31)) return fail(PLSH_ERR_INVALID, "n must be < 2^31");
+  if (q->B * q->H > 65535) return fail(PLSH_ERR_UNSUPPORTED, "B * Hq must be <= 65535");
+  if (bins == nullptr) return fail(PLSH_ERR_INVALID, "bins is NULL");
+  if (bins->n != K->n) return fail(PLSH_ERR_INVALID, "bins were drawn for another n");
+  if (bins->H != q->H) return fail(PLSH_ERR_INVALID, "bins were drawn for another number of heads");
+  if (pos < 0 || pos >= K->n) return fail(PLSH_ERR_INVALID, "pos must be in [0, n)");
+  if ((st = check_bins_device(bins)) != PLSH_OK) return st;
+  plsh::DeviceCtx* ctx = nullptr;
+  if ((st = current_ctx(&ctx)) != PLSH_OK) return st;
+  const size_t bytes =
+      sizeof(float) * plsh::decode_work_floats((int)q->B, (int)q->H, (int)q->d, ctx->num_sms);
+  float* work = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_ctx_mu);
+    if (ctx->decode_work_bytes < bytes) {
+      // grow (the old buffer may still be in use by earlier calls)
+      PLSH_TRY_CUDA(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
+      cudaFree(ctx->decode_work);
+      ctx->decode_work = nullptr;
+      ctx->decode_work_bytes = 0;
+      if ((st = dev_alloc((void**)&ctx->decode_work, bytes, "decode partials")) != PLSH_OK)
+        return st;
+      ctx->decode_work_bytes = bytes;
+    }
+    work = ctx->decode_work;
+  }
+  plsh::DecodeArgs a;
+  a.q = q->data;
+  a.K = K->data;
+  a.V = V->data;
+  a.o = o->data;
+  a.rec = bins->d_rec;
+  a.B = (int)q->B;
+  a.Hq = (int)q->H;
+  a.Hkv = (int)K->H;
+  a.n = (int)K->n;
+  a.d = (int)q->d;
+  a.s = bins->s;
+  a.W = bins->W;
+  a.pos = (int)pos;
+  a.dtype = q->dtype;
+  a.num_sms = ctx->num_sms;
+  a.work = work;
+  PLSH_TRY_CUDA(plsh::launch_decode(a, (cudaStream_t)stream), "decode launch");
+  return PLSH_OK;
+}
+
 plsh_status plsh_alibi_exact(const plsh_tensor* Q, const plsh_tensor* K, const plsh_tensor* V,
                              const double* sigma_h, int32_t causal, plsh_tensor* O,
                              void* stream) {

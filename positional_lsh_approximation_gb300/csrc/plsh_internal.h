@@ -51,6 +51,9 @@ struct DeviceCtx {
   size_t stage_bytes[4] = {0, 0, 0, 0};
   cudaStream_t h2d = nullptr, d2h = nullptr;
   cudaEvent_t ev[2 + 2 * kMaxHostChunks] = {};
+  // per-chunk partial results of the decode step (m, l, P V), grown on demand
+  float* decode_work = nullptr;
+  size_t decode_work_bytes = 0;
 };
 constexpr size_t kMaxTables = 16;
 constexpr int kQueueSlots = 1024;
@@ -101,6 +104,32 @@ struct AttnArgs {
   uint64_t wait_ns;
   int stall;                       // fault injection: the scheduler publishes no item
 };
+
+// decode.cu: one query position against the cached keys; each (batch
+// element, head) is split S ways over its key envelope, a warp per split,
+// S chosen for about 64 warps per SM in all (at most 64 splits)
+inline int decode_splits(int B, int Hq, int num_sms) {
+  const int64_t bh = (int64_t)B * Hq, want = (int64_t)num_sms * 64;
+  const int64_t sp = (want + bh - 1) / bh;
+  return (int)(sp < 1 ? 1 : (sp > 64 ? 64 : sp));
+}
+inline size_t decode_work_floats(int B, int Hq, int d, int num_sms) {
+  return (size_t)B * Hq * decode_splits(B, Hq, num_sms) * (size_t)(d + 2);
+}
+struct DecodeArgs {
+  const void* q;         // [B, Hq, 1, d]
+  const void* K;         // [B, Hkv, n, d]
+  const void* V;
+  void* o;               // [B, Hq, 1, d]
+  const BinRecord* rec;  // [Hq*s][W]
+  int B, Hq, Hkv, n, d, s;
+  int64_t W;
+  int pos;
+  int dtype;             // PLSH_BF16 or PLSH_F32
+  int num_sms;
+  float* work;           // decode_work_floats(B, Hq, d, pos)
+};
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
 
 // attn_simt.cu (CUDA cores, any dtype, d in {64, 128})
 // slopes_host: exact mode, [Hq] log2(e)/sigma_h (at most kMaxExactHeads)
