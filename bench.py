@@ -351,9 +351,44 @@ def run_ours(args, rank, world):
         "clocks": clocks.summary(),
     }
     result["decode"] = measure_decode(w, bins, sigma, flush, stream)
+    result["fixed_blocks"] = measure_fixed(w, sigma, Q, K, V, E, flush, stream)
     if rank == 0 and not args.no_cpu:
         result["cpu_baseline"] = cpu_baseline(w, Qn, Kn, Vn, offsets, starts, args.cpu_seconds)
     return result
+
+
+# ------------------------------------------------------- fixed blocks
+def measure_fixed(w, sigma, Q, K, V, E, flush, stream, iters=10):
+    """The fixed-blocks baseline at the workload's s: blocks of width
+    round(2 sigma_h) (the mean width of the random bins), s evenly shifted
+    grids; attention time on the same kernel and error against exact ALiBi."""
+    import torch
+    import positional_lsh_approximation_gb300 as plsh
+    widths = [max(1, int(round(2.0 * sg))) for sg in sigma]
+    t0 = time.perf_counter()
+    fb = plsh.bins_fixed(w.n, widths, w.s)
+    build_ms = (time.perf_counter() - t0) * 1e3
+    O = torch.empty_like(Q)
+    for _ in range(3):
+        plsh.alibi_attn(Q, K, V, fb, w.causal, out=O)
+    plsh.stream_status()
+    ms = []
+    for _ in range(iters):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        plsh.alibi_attn(Q, K, V, fb, w.causal, out=O)
+        b.record(stream)
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    plsh.stream_status()
+    diff = O.float() - E.float()
+    fb.free()
+    t = statistics.median(ms)
+    return {"widths": "round(2 sigma_h)", "s": w.s, "build_ms": build_ms,
+            "attn_ms": t, "tokens_per_s": w.B * w.n / (t / 1e3),
+            "rel_fro_vs_exact": float(diff.norm() / E.float().norm())}
 
 
 # ------------------------------------------------------------ decode step

@@ -110,6 +110,23 @@ plsh_status plsh_bins_from_host(int64_t n, int32_t H, int32_t s,
 
 /* Shape of a handle.  n_entries (bins + terminals over all hashes) needs the
  * device contents: this call synchronises `stream` when n_entries != NULL. */
+/*
+ * plsh_bins_fixed -- deterministic fixed blocks in place of random hashes (the
+ * "fixed blocks" baseline of the summary's Mistral fine-tuning experiment,
+ * Experimental validation): hash t of head h cuts 0..n-1 into contiguous
+ * blocks of width_h[h] positions, shifted by o = floor(t * width_h[h] / s),
+ * i.e. bin starts {0} u {o + k * width_h[h] : k >= 0} inside [1, n).  With
+ * s = 1 these are plain blocks [0, w), [w, 2w), ...; larger s averages s
+ * evenly shifted grids, the deterministic counterpart of the random offsets.
+ *   width_h: host array [H], every entry >= 1.  1 <= s <= 64, 1 <= n < 2^31.
+ * The records are built on the device in closed form; the call waits for it
+ * (the host arrays it uploads are its own).  The handle is used exactly like
+ * one from plsh_sample_bins (plsh_bins_draws reports w = width, u = o);
+ * plsh_bins_resample on it draws random bins.
+ */
+plsh_status plsh_bins_fixed(int64_t n, const int32_t* width_h, int32_t H, int32_t s,
+                            void* stream, plsh_bins** out);
+
 plsh_status plsh_bins_info(const plsh_bins* bins, int64_t* n, int32_t* H,
                            int32_t* s, int64_t* n_entries, void* stream);
 

@@ -14,6 +14,7 @@ from .oracle import (  # noqa: F401
     draw,
     bins_one,
     sample_bins,
+    bins_fixed,
     plsh_attn_rows,
     plsh_parts_rows,
     alibi_exact_rows,

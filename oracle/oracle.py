@@ -148,6 +148,25 @@ def sample_bins(n: int, sigma, s: int, seed: int, return_draws: bool = False):
     return offsets, starts
 
 
+def bins_fixed(n: int, widths, s: int):
+    """Fixed blocks: hash t of head h has bin starts {0} and every position x
+    in [1, n) with x >= o and (x - o) divisible by w, w = widths[h],
+    o = floor(t * w / s); then the terminal n.  Same layout as sample_bins.
+
+    The fixed-blocks baseline of the summary's fine-tuning experiment
+    (Experimental validation), evaluated position by position.
+    """
+    offsets = [0]
+    starts = []
+    for w in (int(x) for x in widths):
+        for t in range(s):
+            o = t * w // s
+            row = [x for x in range(n) if x == 0 or (x >= o and (x - o) % w == 0)]
+            starts.extend(row + [n])
+            offsets.append(len(starts))
+    return np.asarray(offsets, dtype=np.int64), np.asarray(starts, dtype=np.int32)
+
+
 def _f32(a) -> np.ndarray:
     return np.ascontiguousarray(a, dtype=np.float32)
 

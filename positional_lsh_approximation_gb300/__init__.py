@@ -20,7 +20,7 @@ import torch
 
 from . import build as _build_mod
 
-__all__ = ["build", "load", "sample_bins", "bins_from_host", "Bins", "alibi_attn",
+__all__ = ["build", "load", "sample_bins", "bins_from_host", "bins_fixed", "Bins", "alibi_attn",
            "alibi_attn_noalloc", "alibi_attn_host",
            "alibi_exact", "alibi_decode", "stream_status", "set_wait_limit_ns", "PlshError",
            "library_path"]
@@ -78,6 +78,7 @@ def load():
                                ctypes.POINTER(I32), ctypes.POINTER(I64), P],
             "plsh_bins_to_host": [P, ctypes.POINTER(I64), ctypes.POINTER(I32), I64, P],
             "plsh_bins_draws": [P, D, D, P],
+            "plsh_bins_fixed": [I64, ctypes.POINTER(I32), I32, I32, P, ctypes.POINTER(P)],
             "plsh_alibi_attn": [TP, TP, TP, P, I32, TP, P],
             "plsh_alibi_attn_noalloc": [TP, TP, TP, P, I32, TP, P],
             "plsh_alibi_attn_host": [TP, TP, TP, P, I32, TP, P],
@@ -199,6 +200,16 @@ def bins_from_host(n: int, H: int, s: int, offsets, starts, stream=None) -> Bins
                                       off.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
                                       st.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
                                       _stream(stream), ctypes.byref(out)))
+    return Bins(out.value)
+
+
+def bins_fixed(n: int, widths, s: int, stream=None) -> Bins:
+    """plsh_bins_fixed: deterministic blocks of width widths[h] per head, s
+    grids shifted by floor(t * width / s) (the fixed-blocks baseline)."""
+    wd = np.ascontiguousarray(widths, dtype=np.int32)
+    out = ctypes.c_void_p()
+    _check(load().plsh_bins_fixed(int(n), wd.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                  int(wd.shape[0]), int(s), _stream(stream), ctypes.byref(out)))
     return Bins(out.value)
 
 

@@ -433,6 +433,12 @@ __global__ void noalloc_items_kernel(int4* scratch, const __grid_constant__ NoAl
   }
 }
 
+namespace plsh {
+// sampler.cu: fixed blocks, width d_w[hs] and offset d_u[hs] (integers) for
+// every hash (declared here: only the entry point below launches it)
+cudaError_t launch_bins_fixed(plsh_bins* b, cudaStream_t st);
+}  // namespace plsh
+
 extern "C" {
 
 plsh_status plsh_sample_bins(int64_t n, const double* sigma_h, int32_t H, int32_t s,
@@ -515,6 +521,47 @@ plsh_status plsh_bins_from_host(int64_t n, int32_t H, int32_t s, const int64_t* 
   if (e != cudaSuccess) {
     free_bins(b);
     return cuda_fail(e, "bins upload");
+  }
+  *out = b;
+  return PLSH_OK;
+}
+
+plsh_status plsh_bins_fixed(int64_t n, const int32_t* width_h, int32_t H, int32_t s,
+                            void* stream, plsh_bins** out) {
+  if (out == nullptr || width_h == nullptr) return fail(PLSH_ERR_INVALID, "NULL argument");
+  if (n < 1 || n >= ((int64_t)1 << 31)) return fail(PLSH_ERR_INVALID, "n must be in [1, 2^31)");
+  if (H < 1) return fail(PLSH_ERR_INVALID, "H must be >= 1");
+  if (s < 1 || s > plsh::kMaxS) return fail(PLSH_ERR_INVALID, "s must be in [1, 64]");
+  for (int32_t h = 0; h < H; ++h)
+    if (width_h[h] < 1) return fail(PLSH_ERR_INVALID, "width_h[" + std::to_string(h) + "] must be >= 1");
+  const int64_t HS = (int64_t)H * s;
+  std::vector<double> w(HS), u(HS), sigma_est(H);
+  for (int32_t h = 0; h < H; ++h) {
+    // s grids shifted evenly across one block; blocks of width w cost like
+    // random bins of mean width 2 sigma
+    sigma_est[h] = 0.5 * width_h[h];
+    for (int32_t t = 0; t < s; ++t) {
+      w[(int64_t)h * s + t] = (double)width_h[h];
+      u[(int64_t)h * s + t] = (double)((int64_t)t * width_h[h] / s);
+    }
+  }
+  plsh::DeviceCtx* ctx = nullptr;
+  plsh_status st = current_ctx(&ctx);
+  if (st != PLSH_OK) return st;
+  plsh_bins* b = nullptr;
+  if ((st = new_bins(n, H, s, &b)) != PLSH_OK) return st;
+  b->sigma_host = sigma_est;
+  order_heads(b);
+  cudaStream_t cs = (cudaStream_t)stream;
+  cudaError_t e = cudaMemcpyAsync(b->d_w, w.data(), sizeof(double) * HS, cudaMemcpyHostToDevice, cs);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(b->d_u, u.data(), sizeof(double) * HS, cudaMemcpyHostToDevice, cs);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(b->d_head_order, b->head_order.data(), sizeof(int32_t) * H, cudaMemcpyHostToDevice, cs);
+  if (e == cudaSuccess) e = plsh::launch_bins_fixed(b, cs);
+  // the host arrays above go out of scope: wait for the copies
+  if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
+  if (e != cudaSuccess) {
+    free_bins(b);
+    return cuda_fail(e, "fixed bins");
   }
   *out = b;
   return PLSH_OK;

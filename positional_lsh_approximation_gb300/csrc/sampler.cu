@@ -357,4 +357,42 @@ cudaError_t launch_bins_from_starts(plsh_bins* b, const int32_t* d_starts,
   return cudaGetLastError();
 }
 
+// Fixed blocks (the deterministic baseline the summary's fine-tuning
+// experiment compares against): hash (h, t) cuts 0..n-1 into blocks of width
+// w starting at offset o (integers held in d_w, d_u), starts
+// {0} u {o + k w : k >= 0} inside [1, n).  One thread per record word, in
+// closed form: the word's starts from the first one at or after it, the last
+// start at or before its first position, the first start after it.
+__global__ void fixed_bins_kernel(int n, int64_t W, int64_t HS, const double* __restrict__ d_w,
+                                  const double* __restrict__ d_u, BinRecord* __restrict__ rec) {
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= HS * W) return;
+  const int64_t hs = idx / W;
+  const int wd = (int)(idx - hs * W);
+  // 64-bit positions: a width may be as large as 2^31 - 1
+  const int64_t w = (int64_t)d_w[hs], o = (int64_t)d_u[hs];
+  const int64_t a = (int64_t)wd * 32;
+  uint32_t bits = wd == 0 ? 1u : 0u;
+  for (int64_t p = a <= o ? o : o + (a - o + w - 1) / w * w; p < a + 32 && p < n; p += w)
+    bits |= 1u << (int)(p - a);
+  const int64_t prev = a < o ? 0 : o + (a - o) / w * w;
+  const int64_t z = a + 32;
+  int64_t next = z >= n ? n : (z <= o ? o : o + (z - o + w - 1) / w * w);
+  if (next > n) next = n;
+  BinRecord r;
+  r.bits = bits;
+  r.prev = (int32_t)prev;
+  r.next = (int32_t)next;
+  r.pad = 0;
+  rec[idx] = r;
+}
+
+cudaError_t launch_bins_fixed(plsh_bins* b, cudaStream_t st) {
+  const int64_t HS = (int64_t)b->H * b->s;
+  const int64_t words = HS * b->W;
+  fixed_bins_kernel<<<(unsigned)((words + 255) / 256), 256, 0, st>>>((int)b->n, b->W, HS, b->d_w,
+                                                                      b->d_u, b->d_rec);
+  return cudaGetLastError();
+}
+
 }  // namespace plsh
