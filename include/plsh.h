@@ -42,7 +42,7 @@ typedef enum {
   PLSH_ERR_CUDA = 2,         /* a CUDA runtime/driver call failed           */
   PLSH_ERR_NOMEM = 3,        /* device or host allocation failed            */
   PLSH_ERR_TIMEOUT = 4,      /* a device-side bounded wait ran out          */
-  PLSH_ERR_UNSUPPORTED = 5   /* valid request this build does not serve     */
+  PLSH_ERR_UNSUPPORTED = 5   /* valid request the library does not serve    */
 } plsh_status;
 
 typedef enum { PLSH_F32 = 0, PLSH_BF16 = 1 } plsh_dtype;
