@@ -93,3 +93,36 @@ def test_attention_rejects_null_and_misaligned(lib):
     st = lib.plsh_alibi_exact(ctypes.byref(q3), ctypes.byref(k2), ctypes.byref(k2), sp, 1,
                               ctypes.byref(q3), None)
     assert st == plsh.PLSH_ERR_INVALID
+
+
+def test_decode_rejects_bad_arguments(lib):
+    T = plsh._Tensor
+    q = T(256, plsh.PLSH_BF16, 2, 4, 1, 128)
+    kv = T(256, plsh.PLSH_BF16, 2, 2, 512, 128)
+    o = T(256, plsh.PLSH_BF16, 2, 4, 1, 128)
+
+    def call(q_, k_, v_, o_):
+        return lib.plsh_alibi_decode(ctypes.byref(q_), ctypes.byref(k_), ctypes.byref(v_),
+                                     None, 7, ctypes.byref(o_), None)
+    assert call(q, kv, kv, o) == plsh.PLSH_ERR_INVALID                       # bins NULL
+    assert call(T(256, plsh.PLSH_BF16, 2, 4, 2, 128), kv, kv, o) == plsh.PLSH_ERR_INVALID
+    assert call(T(258, plsh.PLSH_BF16, 2, 4, 1, 128), kv, kv, o) == plsh.PLSH_ERR_INVALID
+    assert call(q, T(256, plsh.PLSH_F32, 2, 2, 512, 128), kv, o) == plsh.PLSH_ERR_INVALID
+    assert call(q, T(256, plsh.PLSH_BF16, 2, 3, 512, 128),
+                T(256, plsh.PLSH_BF16, 2, 3, 512, 128), o) == plsh.PLSH_ERR_INVALID
+    assert call(q, kv, kv, T(256, plsh.PLSH_BF16, 2, 4, 1, 64)) == plsh.PLSH_ERR_INVALID
+    assert call(q, kv, T(256, plsh.PLSH_BF16, 2, 2, 511, 128), o) == plsh.PLSH_ERR_INVALID
+
+
+@pytest.mark.parametrize("n,widths,s", [(0, [4], 1), (10, [], 1), (10, [4], 0),
+                                        (10, [4], 65), (10, [4, 0], 2), (10, [-3], 1)])
+def test_bins_fixed_rejects_bad_arguments(lib, n, widths, s):
+    wd = np.asarray(widths if widths else [1], dtype=np.int32)
+    H = len(widths)
+    out = ctypes.c_void_p()
+    st = lib.plsh_bins_fixed(n, wd.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), H, s,
+                             None, ctypes.byref(out))
+    assert st == plsh.PLSH_ERR_INVALID
+    assert out.value is None
+    st = lib.plsh_bins_fixed(10, None, 1, 1, None, ctypes.byref(out))
+    assert st == plsh.PLSH_ERR_INVALID
