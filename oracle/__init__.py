@@ -15,6 +15,7 @@ from .oracle import (  # noqa: F401
     bins_one,
     sample_bins,
     bins_fixed,
+    bias_error,
     plsh_attn_rows,
     plsh_parts_rows,
     alibi_exact_rows,

@@ -167,6 +167,27 @@ def bins_fixed(n: int, widths, s: int):
     return np.asarray(offsets, dtype=np.int64), np.asarray(starts, dtype=np.int32)
 
 
+def bias_error(n: int, sigma: float, offsets, starts, h: int, s: int):
+    """||L* - M~||_max and ||L* - M~||_2 for head h, as dense fp64 matrices.
+
+    L*_ij = e^{-|i-j|/sigma} (Problem statement) and M~ = (1/s) sum_t M(h_t),
+    M(h_t)_ij = 1 when i and j share a bin of hash t (Methodology 1-2); the
+    summary's convergence experiment measures these two norms against s.
+    Small n only (n x n matrices); the spectral norm of the symmetric
+    difference is its largest eigenvalue magnitude.
+    """
+    pos = np.arange(n)
+    m = np.zeros((n, n))
+    for t in range(s):
+        st = np.asarray(starts[offsets[h * s + t]:offsets[h * s + t + 1]])
+        ids = np.searchsorted(st, pos, side="right")
+        m += (ids[:, None] == ids[None, :])
+    m /= s
+    L = np.exp(-np.abs(pos[:, None] - pos[None, :]) / float(sigma))
+    E = L - m
+    return float(np.abs(E).max()), float(np.abs(np.linalg.eigvalsh(E)).max())
+
+
 def _f32(a) -> np.ndarray:
     return np.ascontiguousarray(a, dtype=np.float32)
 

@@ -235,9 +235,14 @@ def test_error_decays_as_inverse_sqrt_s():
         sp, mm = [], []
         for seed in range(8):
             offsets, starts = oracle.sample_bins(n, [sigma], s, seed=100 + seed)
-            E = dense_mask_mean(n, offsets, starts, 0, s) - L
-            sp.append(np.abs(np.linalg.eigvalsh(E)).max())
-            mm.append(np.abs(E).max())
+            e_max, e_spec = oracle.bias_error(n, sigma, offsets, starts, 0, s)
+            if seed == 0:
+                # the oracle's norms are those of the test's own dense matrices
+                E = dense_mask_mean(n, offsets, starts, 0, s) - L
+                assert abs(e_max - np.abs(E).max()) < 1e-14
+                assert abs(e_spec - np.abs(np.linalg.eigvalsh(E)).max()) < 1e-12
+            sp.append(e_spec)
+            mm.append(e_max)
         spec.append(np.mean(sp)); mx.append(np.mean(mm))
     slope_spec = np.polyfit(np.log(ss), np.log(spec), 1)[0]
     slope_max = np.polyfit(np.log(ss[2:]), np.log(mx[2:]), 1)[0]
@@ -412,3 +417,39 @@ def test_numerator_and_denominator_are_unbiased():
     se_den = dens.std(axis=0, ddof=1) / math.sqrt(blocks)
     assert np.all(np.abs(nums.mean(0) - ref_num) <= 5 * se_num + 1e-9)
     assert np.all(np.abs(dens.mean(0) - ref_den) <= 5 * se_den + 1e-9)
+
+
+def test_bias_error_closed_forms():
+    """||L* - M~|| in two cases with closed forms.  All singletons: M~ = I, so
+    the max-norm error is the nearest off-diagonal entry e^{-1/sigma} and the
+    spectral error is max |lambda(L*) - 1| = coth(1/(2 sigma)) - 1 in the
+    Toeplitz limit (Kac-Murdock-Szego).  One bin over everything: M~ = 1 1^T,
+    the max-norm error is the far corner 1 - e^{-(n-1)/sigma}."""
+    n, sigma, s = 1500, 8.0, 3
+    offsets = np.arange(0, s * (n + 1) + 1, n + 1, dtype=np.int64)
+    starts = np.tile(np.arange(n + 1, dtype=np.int32), s)
+    e_max, e_spec = oracle.bias_error(n, sigma, offsets, starts, 0, s)
+    assert abs(e_max - math.exp(-1.0 / sigma)) < 1e-14
+    assert abs(e_spec / (1.0 / math.tanh(0.5 / sigma) - 1.0) - 1.0) < 5e-3
+    offsets = np.array([0, 2, 4], dtype=np.int64)
+    starts = np.array([0, 300, 0, 300], dtype=np.int32)
+    e_max, _ = oracle.bias_error(300, 40.0, offsets, starts, 0, 2)
+    assert abs(e_max - (1.0 - math.exp(-299.0 / 40.0))) < 1e-14
+
+
+def test_bias_error_brute_force():
+    """The oracle's max-norm error against an entry-by-entry loop on a tiny case."""
+    n, sigma, s = 23, 3.0, 4
+    offsets, starts = oracle.sample_bins(n, [sigma], s, seed=9)
+    e_max, _ = oracle.bias_error(n, sigma, offsets, starts, 0, s)
+    best = 0.0
+    for i in range(n):
+        for j in range(n):
+            c = 0
+            for t in range(s):
+                st = list(starts[offsets[t]:offsets[t + 1]])
+                bi = max(k for k in range(len(st) - 1) if st[k] <= i)
+                bj = max(k for k in range(len(st) - 1) if st[k] <= j)
+                c += bi == bj
+            best = max(best, abs(math.exp(-abs(i - j) / sigma) - c / s))
+    assert abs(e_max - best) < 1e-15
