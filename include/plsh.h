@@ -127,6 +127,25 @@ plsh_status plsh_bins_from_host(int64_t n, int32_t H, int32_t s,
 plsh_status plsh_bins_fixed(int64_t n, const int32_t* width_h, int32_t H, int32_t s,
                             void* stream, plsh_bins** out);
 
+/*
+ * plsh_bias_error -- the bias of the averaged mask for head h of `bins`:
+ * ||L* - M~||_max and ||L* - M~||_2 with L*_ij = e^{-|i-j|/sigma} (Problem
+ * statement) and M~ = (1/s) sum_t M(h_t) (Methodology 1-2), the two norms the
+ * summary's convergence experiment follows against s (Results).  Neither
+ * n x n matrix is formed: the max norm is exact (per row over its key
+ * envelope); the spectral norm, the largest eigenvalue magnitude of the
+ * symmetric difference, is estimated by `lanczos_iters` Lanczos steps from a
+ * start vector drawn from `seed`, with O(n s) products (the Laplace kernel as
+ * two linear recurrences, the mask through prefix sums).  fp64 throughout.
+ *   sigma > 0 (the scale L* is taken at), 0 <= h < H,
+ *   2 <= lanczos_iters <= 1000 when spectral is requested.
+ *   max_abs, spectral: host outputs; either may be NULL to skip it.
+ * Blocks until done (device scratch of 6 n doubles, allocated per call).
+ */
+plsh_status plsh_bias_error(const plsh_bins* bins, double sigma, int32_t h,
+                            int32_t lanczos_iters, uint64_t seed, double* max_abs,
+                            double* spectral, void* stream);
+
 plsh_status plsh_bins_info(const plsh_bins* bins, int64_t* n, int32_t* H,
                            int32_t* s, int64_t* n_entries, void* stream);
 

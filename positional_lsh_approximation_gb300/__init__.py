@@ -22,7 +22,7 @@ from . import build as _build_mod
 
 __all__ = ["build", "load", "sample_bins", "bins_from_host", "bins_fixed", "Bins", "alibi_attn",
            "alibi_attn_noalloc", "alibi_attn_host",
-           "alibi_exact", "alibi_decode", "stream_status", "set_wait_limit_ns", "PlshError",
+           "alibi_exact", "alibi_decode", "bias_error", "stream_status", "set_wait_limit_ns", "PlshError",
            "library_path"]
 
 PLSH_OK, PLSH_ERR_INVALID, PLSH_ERR_CUDA, PLSH_ERR_NOMEM, PLSH_ERR_TIMEOUT, \
@@ -79,6 +79,7 @@ def load():
             "plsh_bins_to_host": [P, ctypes.POINTER(I64), ctypes.POINTER(I32), I64, P],
             "plsh_bins_draws": [P, D, D, P],
             "plsh_bins_fixed": [I64, ctypes.POINTER(I32), I32, I32, P, ctypes.POINTER(P)],
+            "plsh_bias_error": [P, ctypes.c_double, I32, I32, U64, D, D, P],
             "plsh_alibi_attn": [TP, TP, TP, P, I32, TP, P],
             "plsh_alibi_attn_noalloc": [TP, TP, TP, P, I32, TP, P],
             "plsh_alibi_attn_host": [TP, TP, TP, P, I32, TP, P],
@@ -298,6 +299,16 @@ def alibi_decode(q, K, V, bins: Bins, pos: int, out=None, stream=None):
     _check(load().plsh_alibi_decode(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv),
                                     bins.handle, int(pos), ctypes.byref(to), _stream(stream)))
     return o
+
+
+def bias_error(bins: Bins, sigma: float, h: int, lanczos_iters: int = 60, seed: int = 0,
+               stream=None):
+    """plsh_bias_error: (||L* - M~||_max, ||L* - M~||_2) for head h."""
+    mx, sp = ctypes.c_double(), ctypes.c_double()
+    _check(load().plsh_bias_error(bins.handle, float(sigma), int(h), int(lanczos_iters),
+                                  int(seed) & (2**64 - 1), ctypes.byref(mx), ctypes.byref(sp),
+                                  _stream(stream)))
+    return mx.value, sp.value
 
 
 def stream_status(stream=None):

@@ -437,6 +437,9 @@ namespace plsh {
 // sampler.cu: fixed blocks, width d_w[hs] and offset d_u[hs] (integers) for
 // every hash (declared here: only the entry point below launches it)
 cudaError_t launch_bins_fixed(plsh_bins* b, cudaStream_t st);
+// bias.cu: ||L* - M~|| in max and spectral norm for one head
+cudaError_t bias_error(const plsh_bins* bn, double sigma, int h, int iters, uint64_t seed,
+                       double* max_abs, double* spectral, cudaStream_t st);
 }  // namespace plsh
 
 extern "C" {
@@ -564,6 +567,24 @@ plsh_status plsh_bins_fixed(int64_t n, const int32_t* width_h, int32_t H, int32_
     return cuda_fail(e, "fixed bins");
   }
   *out = b;
+  return PLSH_OK;
+}
+
+plsh_status plsh_bias_error(const plsh_bins* bins, double sigma, int32_t h,
+                            int32_t lanczos_iters, uint64_t seed, double* max_abs,
+                            double* spectral, void* stream) {
+  if (bins == nullptr) return fail(PLSH_ERR_INVALID, "bins is NULL");
+  if (max_abs == nullptr && spectral == nullptr)
+    return fail(PLSH_ERR_INVALID, "nothing to compute: max_abs and spectral are NULL");
+  if (!(sigma > 0.0) || !isfinite(sigma)) return fail(PLSH_ERR_INVALID, "sigma must be finite and > 0");
+  if (h < 0 || h >= bins->H) return fail(PLSH_ERR_INVALID, "h must be in [0, H)");
+  if (spectral != nullptr && (lanczos_iters < 2 || lanczos_iters > 1000))
+    return fail(PLSH_ERR_INVALID, "lanczos_iters must be in [2, 1000]");
+  plsh_status st = check_bins_device(bins);
+  if (st != PLSH_OK) return st;
+  PLSH_TRY_CUDA(plsh::bias_error(bins, sigma, h, lanczos_iters, seed, max_abs, spectral,
+                                 (cudaStream_t)stream),
+                "bias error");
   return PLSH_OK;
 }
 

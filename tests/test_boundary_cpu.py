@@ -126,3 +126,9 @@ def test_bins_fixed_rejects_bad_arguments(lib, n, widths, s):
     assert out.value is None
     st = lib.plsh_bins_fixed(10, None, 1, 1, None, ctypes.byref(out))
     assert st == plsh.PLSH_ERR_INVALID
+
+
+def test_bias_error_rejects_null_arguments(lib):
+    mx, sp = ctypes.c_double(), ctypes.c_double()
+    st = lib.plsh_bias_error(None, 8.0, 0, 60, 0, ctypes.byref(mx), ctypes.byref(sp), None)
+    assert st == plsh.PLSH_ERR_INVALID
