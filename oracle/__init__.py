@@ -17,6 +17,7 @@ from .oracle import (  # noqa: F401
     bins_fixed,
     bias_error,
     plsh_attn_rows,
+    plsh_attn_backward,
     plsh_parts_rows,
     alibi_exact_rows,
     set_threads,

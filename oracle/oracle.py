@@ -7,6 +7,7 @@ follows; the arithmetic itself lives in plsh_oracle.c.
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 import subprocess
 import threading
@@ -186,6 +187,54 @@ def bias_error(n: int, sigma: float, offsets, starts, h: int, s: int):
     L = np.exp(-np.abs(pos[:, None] - pos[None, :]) / float(sigma))
     E = L - m
     return float(np.abs(E).max()), float(np.abs(np.linalg.eigvalsh(E)).max())
+
+
+def plsh_attn_backward(Q, K, V, dO, offsets, starts, s: int, causal: bool):
+    """Gradients (dQ, dK, dV) of the approximation with respect to its inputs,
+    fp64, dense per (batch, head); small n only.
+
+    Row i of the forward is O_i = sum_j P_ij v_j with P_ij = w_ij / sum_j w_ij,
+    w_ij = c_ij e^{S_ij}, S_ij = q_i . k_j / sqrt(d) and c_ij the number of
+    hashes that put i and j in one bin (Methodology 3: numerator and row sums
+    averaged over the masks); c does not depend on Q, K, V.  The chain rule
+    gives dV_j = sum_i P_ij dO_i, dP_ij = dO_i . v_j,
+    dS_ij = P_ij (dP_ij - sum_l P_il dP_il), dQ_i = sum_j dS_ij k_j / sqrt(d),
+    dK_j = sum_i dS_ij q_i / sqrt(d); a KV head collects the gradients of all
+    the query heads that read it.
+    """
+    Q = np.asarray(Q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    V = np.asarray(V, dtype=np.float64)
+    dO = np.asarray(dO, dtype=np.float64)
+    B, Hq, n, d = Q.shape
+    Hkv = K.shape[1]
+    group = Hq // Hkv
+    pos = np.arange(n)
+    dQ = np.zeros_like(Q)
+    dK = np.zeros_like(K)
+    dV = np.zeros_like(V)
+    for h in range(Hq):
+        c = np.zeros((n, n))
+        for t in range(s):
+            st = np.asarray(starts[offsets[h * s + t]:offsets[h * s + t + 1]])
+            ids = np.searchsorted(st, pos, side="right")
+            c += (ids[:, None] == ids[None, :])
+        if causal:
+            c = np.tril(c)
+        for b in range(B):
+            q, k, v = Q[b, h], K[b, h // group], V[b, h // group]
+            S = q @ k.T / math.sqrt(d)
+            live = c > 0
+            Sm = np.where(live, S, -np.inf)
+            w = c * np.exp(Sm - Sm.max(axis=1, keepdims=True))
+            P = w / w.sum(axis=1, keepdims=True)
+            g = dO[b, h]
+            dP = g @ v.T
+            dS = P * (dP - (P * dP).sum(axis=1, keepdims=True))
+            dV[b, h // group] += P.T @ g
+            dQ[b, h] = dS @ k / math.sqrt(d)
+            dK[b, h // group] += dS.T @ q / math.sqrt(d)
+    return dQ, dK, dV
 
 
 def _f32(a) -> np.ndarray:
