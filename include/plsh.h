@@ -128,6 +128,27 @@ plsh_status plsh_bins_fixed(int64_t n, const int32_t* width_h, int32_t H, int32_
                             void* stream, plsh_bins** out);
 
 /*
+ * plsh_alibi_attn_backward -- gradients of sum(T~ * dO) with respect to Q, K
+ * and V (the backward pass of plsh_alibi_attn, Methodology 3's estimator with
+ * the multiplicities c_ij held fixed):
+ *   P_ij = c_ij e^{S_ij} / sum_j c_ij e^{S_ij},  dP_ij = dO_i . v_j,
+ *   dS_ij = P_ij (dP_ij - sum_l P_il dP_il),
+ *   dQ_i = sum_j dS_ij k_j / sqrt(d),  dK_j = sum_i dS_ij q_i / sqrt(d),
+ *   dV_j = sum_i P_ij dO_i,
+ * a KV head collecting the sums of every query head that reads it.
+ *   Q, dO, dQ [B,Hq,n,d]; K, V, dK, dV [B,Hkv,n,d]; one dtype (PLSH_BF16 or
+ *   PLSH_F32), d in {64, 128}; bins and causal as for plsh_alibi_attn.
+ * CUDA cores, fp32 accumulation, no atomics: a warp per row computes the
+ * row's max, sum and sum_j P_ij dP_ij (kept in stream-ordered scratch of
+ * 3 B Hq n floats) and dQ_i; a warp per key then sums dK_j and dV_j over the
+ * rows whose bins contain it.  Asynchronous on `stream`.
+ */
+plsh_status plsh_alibi_attn_backward(const plsh_tensor* Q, const plsh_tensor* K,
+                                     const plsh_tensor* V, const plsh_tensor* dO,
+                                     const plsh_bins* bins, int32_t causal, plsh_tensor* dQ,
+                                     plsh_tensor* dK, plsh_tensor* dV, void* stream);
+
+/*
  * plsh_bias_error -- the bias of the averaged mask for head h of `bins`:
  * ||L* - M~||_max and ||L* - M~||_2 with L*_ij = e^{-|i-j|/sigma} (Problem
  * statement) and M~ = (1/s) sum_t M(h_t) (Methodology 1-2), the two norms the

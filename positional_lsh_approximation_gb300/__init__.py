@@ -22,7 +22,7 @@ from . import build as _build_mod
 
 __all__ = ["build", "load", "sample_bins", "bins_from_host", "bins_fixed", "Bins", "alibi_attn",
            "alibi_attn_noalloc", "alibi_attn_host",
-           "alibi_exact", "alibi_decode", "bias_error", "stream_status", "set_wait_limit_ns", "PlshError",
+           "alibi_exact", "alibi_decode", "alibi_attn_backward", "bias_error", "stream_status", "set_wait_limit_ns", "PlshError",
            "library_path"]
 
 PLSH_OK, PLSH_ERR_INVALID, PLSH_ERR_CUDA, PLSH_ERR_NOMEM, PLSH_ERR_TIMEOUT, \
@@ -80,6 +80,7 @@ def load():
             "plsh_bins_draws": [P, D, D, P],
             "plsh_bins_fixed": [I64, ctypes.POINTER(I32), I32, I32, P, ctypes.POINTER(P)],
             "plsh_bias_error": [P, ctypes.c_double, I32, I32, U64, D, D, P],
+            "plsh_alibi_attn_backward": [TP, TP, TP, TP, P, I32, TP, TP, TP, P],
             "plsh_alibi_attn": [TP, TP, TP, P, I32, TP, P],
             "plsh_alibi_attn_noalloc": [TP, TP, TP, P, I32, TP, P],
             "plsh_alibi_attn_host": [TP, TP, TP, P, I32, TP, P],
@@ -299,6 +300,17 @@ def alibi_decode(q, K, V, bins: Bins, pos: int, out=None, stream=None):
     _check(load().plsh_alibi_decode(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv),
                                     bins.handle, int(pos), ctypes.byref(to), _stream(stream)))
     return o
+
+
+def alibi_attn_backward(Q, K, V, dO, bins: Bins, causal: bool, stream=None):
+    """plsh_alibi_attn_backward: (dQ, dK, dV) of sum(T~ * dO), device tensors."""
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    t = [_desc(x) for x in (Q, K, V, dO, dQ, dK, dV)]
+    _check(load().plsh_alibi_attn_backward(
+        ctypes.byref(t[0]), ctypes.byref(t[1]), ctypes.byref(t[2]), ctypes.byref(t[3]),
+        bins.handle, int(bool(causal)), ctypes.byref(t[4]), ctypes.byref(t[5]),
+        ctypes.byref(t[6]), _stream(stream)))
+    return dQ, dK, dV
 
 
 def bias_error(bins: Bins, sigma: float, h: int, lanczos_iters: int = 60, seed: int = 0,

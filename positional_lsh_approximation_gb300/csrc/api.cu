@@ -440,6 +440,10 @@ cudaError_t launch_bins_fixed(plsh_bins* b, cudaStream_t st);
 // bias.cu: ||L* - M~|| in max and spectral norm for one head
 cudaError_t bias_error(const plsh_bins* bn, double sigma, int h, int iters, uint64_t seed,
                        double* max_abs, double* spectral, cudaStream_t st);
+// bwd.cu: gradients of the approximation
+cudaError_t launch_attn_bwd(const void* Q, const void* K, const void* V, const void* dO, void* dQ,
+                            void* dK, void* dV, float* stats, const plsh_bins* bn, int B, int Hq,
+                            int Hkv, int n, int d, int causal, int dtype, cudaStream_t st);
 }  // namespace plsh
 
 extern "C" {
@@ -567,6 +571,39 @@ plsh_status plsh_bins_fixed(int64_t n, const int32_t* width_h, int32_t H, int32_
     return cuda_fail(e, "fixed bins");
   }
   *out = b;
+  return PLSH_OK;
+}
+
+plsh_status plsh_alibi_attn_backward(const plsh_tensor* Q, const plsh_tensor* K,
+                                     const plsh_tensor* V, const plsh_tensor* dO,
+                                     const plsh_bins* bins, int32_t causal, plsh_tensor* dQ,
+                                     plsh_tensor* dK, plsh_tensor* dV, void* stream) {
+  plsh_status st = check_qkvo(Q, K, V, dO);
+  if (st != PLSH_OK) return st;
+  if ((st = check_tensor(dQ, "dQ")) != PLSH_OK || (st = check_tensor(dK, "dK")) != PLSH_OK ||
+      (st = check_tensor(dV, "dV")) != PLSH_OK)
+    return st;
+  if (dQ->dtype != Q->dtype || dK->dtype != Q->dtype || dV->dtype != Q->dtype)
+    return fail(PLSH_ERR_INVALID, "dQ, dK and dV must have Q's dtype");
+  if (dQ->B != Q->B || dQ->H != Q->H || dQ->n != Q->n || dQ->d != Q->d)
+    return fail(PLSH_ERR_INVALID, "dQ must have Q's shape");
+  if (dK->B != K->B || dK->H != K->H || dK->n != K->n || dK->d != K->d ||
+      dV->B != K->B || dV->H != K->H || dV->n != K->n || dV->d != K->d)
+    return fail(PLSH_ERR_INVALID, "dK and dV must have K's shape");
+  if (bins == nullptr) return fail(PLSH_ERR_INVALID, "bins is NULL");
+  if (bins->n != Q->n) return fail(PLSH_ERR_INVALID, "bins were drawn for another n");
+  if (bins->H != Q->H) return fail(PLSH_ERR_INVALID, "bins were drawn for another number of heads");
+  if ((st = check_bins_device(bins)) != PLSH_OK) return st;
+  cudaStream_t cs = (cudaStream_t)stream;
+  float* stats = nullptr;
+  const size_t bytes = sizeof(float) * 3 * (size_t)Q->B * Q->H * Q->n;
+  PLSH_TRY_CUDA(cudaMallocAsync((void**)&stats, bytes, cs), "backward scratch");
+  cudaError_t e = plsh::launch_attn_bwd(Q->data, K->data, V->data, dO->data, dQ->data, dK->data,
+                                        dV->data, stats, bins, (int)Q->B, (int)Q->H, (int)K->H,
+                                        (int)Q->n, (int)Q->d, causal ? 1 : 0, Q->dtype, cs);
+  const cudaError_t ef = cudaFreeAsync(stats, cs);
+  if (e == cudaSuccess) e = ef;
+  PLSH_TRY_CUDA(e, "backward launch");
   return PLSH_OK;
 }
 

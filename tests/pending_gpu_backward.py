@@ -1,0 +1,55 @@
+"""GPU checks of plsh_alibi_attn_backward against the oracle's gradients,
+written for the GB300 run that first verifies the entry point (rename to
+test_*.py then).  fp32 inputs: 1e-4 relative to the largest gradient entry;
+bf16 inputs: the gradients are rounded to bf16, 1e-2 of that scale."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import positional_lsh_approximation_gb300 as plsh
+from positional_lsh_approximation_gb300.inputs import Workload, make_qkv
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    plsh.build()
+    plsh.load()
+
+
+CASES = [
+    # name, B, Hq, Hkv, n, d, dtype, causal, s, sigma
+    ("f32_causal_gqa", 2, 4, 2, 260, 128, "f32", True, 5, (0.7, 3.0, 20.0, 90.0)),
+    ("f32_noncausal", 1, 2, 1, 300, 64, "f32", False, 6, (2.0, 40.0)),
+    ("bf16_causal", 1, 4, 2, 400, 128, "bf16", True, 10, (1.2, 6.0, 40.0, 300.0)),
+    ("bf16_noncausal_d64", 1, 2, 2, 333, 64, "bf16", False, 4, (5.0, 60.0)),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_backward_matches_oracle(case):
+    name, B, Hq, Hkv, n, d, dtype, causal, s, sig = case
+    w = Workload(name, B, Hq, Hkv, n, d, dtype, causal, s, sig, qkv_seed=n + d)
+    Q, K, V = make_qkv(w)
+    rng = np.random.default_rng(n)
+    dO = rng.standard_normal(Q.shape).astype(np.float32)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    if dtype == "bf16":
+        dO = torch.from_numpy(dO).to(tdt).float().numpy()
+    bins = plsh.sample_bins(n, w.sigmas(), s, seed=6)
+    off, st = oracle.sample_bins(n, w.sigmas(), s, seed=6)
+    dev = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(tdt).cuda()
+    dQ, dK, dV = plsh.alibi_attn_backward(dev(Q), dev(K), dev(V), dev(dO), bins, causal)
+    plsh.stream_status()
+    ref = oracle.plsh_attn_backward(Q, K, V, dO, off, st, s, causal)
+    rel = 1e-4 if dtype == "f32" else 1e-2
+    for got, want, what in zip((dQ, dK, dV), ref, ("dQ", "dK", "dV")):
+        g = got.float().cpu().numpy().astype(np.float64)
+        scale = np.abs(want).max()
+        err = np.abs(g - want).max()
+        assert err <= rel * scale, f"{name} {what}: max err {err:.3e} vs scale {scale:.3e}"
+    bins.free()

@@ -132,3 +132,19 @@ def test_bias_error_rejects_null_arguments(lib):
     mx, sp = ctypes.c_double(), ctypes.c_double()
     st = lib.plsh_bias_error(None, 8.0, 0, 60, 0, ctypes.byref(mx), ctypes.byref(sp), None)
     assert st == plsh.PLSH_ERR_INVALID
+
+
+def test_backward_rejects_bad_arguments(lib):
+    T = plsh._Tensor
+    q = T(256, plsh.PLSH_BF16, 1, 2, 128, 128)
+    k = T(256, plsh.PLSH_BF16, 1, 1, 128, 128)
+    bad = T(256, plsh.PLSH_BF16, 1, 2, 64, 128)
+
+    def call(dq, dk, dv):
+        return lib.plsh_alibi_attn_backward(ctypes.byref(q), ctypes.byref(k), ctypes.byref(k),
+                                            ctypes.byref(q), None, 1, ctypes.byref(dq),
+                                            ctypes.byref(dk), ctypes.byref(dv), None)
+    assert call(q, k, k) == plsh.PLSH_ERR_INVALID          # bins NULL
+    assert call(bad, k, k) == plsh.PLSH_ERR_INVALID        # dQ shape
+    assert call(q, q, k) == plsh.PLSH_ERR_INVALID          # dK shape
+    assert call(q, k, T(256, plsh.PLSH_F32, 1, 1, 128, 128)) == plsh.PLSH_ERR_INVALID
