@@ -167,6 +167,19 @@ plsh_status plsh_bias_error(const plsh_bins* bins, double sigma, int32_t h,
                             int32_t lanczos_iters, uint64_t seed, double* max_abs,
                             double* spectral, void* stream);
 
+/*
+ * plsh_bins_share_groups -- hashes shared across a GQA group: bins for Hq
+ * query heads in which head h uses every hash (records, draws and scale) of
+ * head floor(h / (Hq / G)) of `src`, G = src's number of heads, Hq % G == 0.
+ * Drawn with one scale per KV group (plsh_sample_bins with G heads), the heads
+ * of a group then cut the positions identically, so the key envelopes of two
+ * heads of one group coincide.  A variant outside the summary's method (each
+ * of its heads draws its own hashes).  Device-to-device copies; the call
+ * waits for them.  plsh_bins_resample on the result draws per-head hashes.
+ */
+plsh_status plsh_bins_share_groups(const plsh_bins* src, int32_t Hq, void* stream,
+                                   plsh_bins** out);
+
 plsh_status plsh_bins_info(const plsh_bins* bins, int64_t* n, int32_t* H,
                            int32_t* s, int64_t* n_entries, void* stream);
 

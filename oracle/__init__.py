@@ -15,6 +15,7 @@ from .oracle import (  # noqa: F401
     bins_one,
     sample_bins,
     bins_fixed,
+    share_groups,
     bias_error,
     plsh_attn_rows,
     plsh_attn_backward,

@@ -168,6 +168,22 @@ def bins_fixed(n: int, widths, s: int):
     return np.asarray(offsets, dtype=np.int64), np.asarray(starts, dtype=np.int32)
 
 
+def share_groups(offsets, starts, G: int, Hq: int, s: int):
+    """Start lists for Hq heads where head h uses the s hashes of head
+    h // (Hq // G) of the given lists (G heads): hashes shared across a GQA
+    group.  Same layout as sample_bins."""
+    group = Hq // G
+    out_off = [0]
+    out_st = []
+    for h in range(Hq):
+        g = h // group
+        for t in range(s):
+            row = list(starts[offsets[g * s + t]:offsets[g * s + t + 1]])
+            out_st.extend(row)
+            out_off.append(len(out_st))
+    return np.asarray(out_off, dtype=np.int64), np.asarray(out_st, dtype=np.int32)
+
+
 def bias_error(n: int, sigma: float, offsets, starts, h: int, s: int):
     """||L* - M~||_max and ||L* - M~||_2 for head h, as dense fp64 matrices.
 

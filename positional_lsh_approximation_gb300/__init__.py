@@ -20,7 +20,7 @@ import torch
 
 from . import build as _build_mod
 
-__all__ = ["build", "load", "sample_bins", "bins_from_host", "bins_fixed", "Bins", "alibi_attn",
+__all__ = ["build", "load", "sample_bins", "bins_from_host", "bins_fixed", "bins_share_groups", "Bins", "alibi_attn",
            "alibi_attn_noalloc", "alibi_attn_host",
            "alibi_exact", "alibi_decode", "alibi_attn_backward", "bias_error", "stream_status", "set_wait_limit_ns", "PlshError",
            "library_path"]
@@ -79,6 +79,7 @@ def load():
             "plsh_bins_to_host": [P, ctypes.POINTER(I64), ctypes.POINTER(I32), I64, P],
             "plsh_bins_draws": [P, D, D, P],
             "plsh_bins_fixed": [I64, ctypes.POINTER(I32), I32, I32, P, ctypes.POINTER(P)],
+            "plsh_bins_share_groups": [P, I32, P, ctypes.POINTER(P)],
             "plsh_bias_error": [P, ctypes.c_double, I32, I32, U64, D, D, P],
             "plsh_alibi_attn_backward": [TP, TP, TP, TP, P, I32, TP, TP, TP, P],
             "plsh_alibi_attn": [TP, TP, TP, P, I32, TP, P],
@@ -212,6 +213,14 @@ def bins_fixed(n: int, widths, s: int, stream=None) -> Bins:
     out = ctypes.c_void_p()
     _check(load().plsh_bins_fixed(int(n), wd.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
                                   int(wd.shape[0]), int(s), _stream(stream), ctypes.byref(out)))
+    return Bins(out.value)
+
+
+def bins_share_groups(src: Bins, Hq: int, stream=None) -> Bins:
+    """plsh_bins_share_groups: head h of the result uses the hashes of head
+    h // (Hq // G) of `src` (G heads)."""
+    out = ctypes.c_void_p()
+    _check(load().plsh_bins_share_groups(src.handle, int(Hq), _stream(stream), ctypes.byref(out)))
     return Bins(out.value)
 
 

@@ -625,6 +625,50 @@ plsh_status plsh_bias_error(const plsh_bins* bins, double sigma, int32_t h,
   return PLSH_OK;
 }
 
+plsh_status plsh_bins_share_groups(const plsh_bins* src, int32_t Hq, void* stream,
+                                   plsh_bins** out) {
+  if (src == nullptr || out == nullptr) return fail(PLSH_ERR_INVALID, "NULL argument");
+  if (Hq < 1 || Hq % src->H != 0)
+    return fail(PLSH_ERR_INVALID, "Hq must be a positive multiple of the source's heads");
+  plsh_status st = check_bins_device(src);
+  if (st != PLSH_OK) return st;
+  plsh_bins* b = nullptr;
+  if ((st = new_bins(src->n, Hq, src->s, &b)) != PLSH_OK) return st;
+  const int32_t group = Hq / src->H;
+  const int64_t s = src->s;
+  b->sigma_host.resize(Hq);
+  for (int32_t h = 0; h < Hq; ++h) b->sigma_host[h] = src->sigma_host[h / group];
+  order_heads(b);
+  cudaStream_t cs = (cudaStream_t)stream;
+  cudaError_t e = cudaSuccess;
+  // head h takes every record, draw and scale of head h / group of src
+  for (int32_t h = 0; h < Hq && e == cudaSuccess; ++h) {
+    const int32_t g = h / group;
+    e = cudaMemcpyAsync(b->d_rec + (int64_t)h * s * b->W, src->d_rec + (int64_t)g * s * src->W,
+                        sizeof(plsh::BinRecord) * s * src->W, cudaMemcpyDeviceToDevice, cs);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(b->d_w + h * s, src->d_w + g * s, sizeof(double) * s,
+                          cudaMemcpyDeviceToDevice, cs);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(b->d_u + h * s, src->d_u + g * s, sizeof(double) * s,
+                          cudaMemcpyDeviceToDevice, cs);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(b->d_sigma + h, src->d_sigma + g, sizeof(double),
+                          cudaMemcpyDeviceToDevice, cs);
+  }
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(b->d_head_order, b->head_order.data(), sizeof(int32_t) * Hq,
+                        cudaMemcpyHostToDevice, cs);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
+  if (e != cudaSuccess) {
+    free_bins(b);
+    return cuda_fail(e, "shared bins");
+  }
+  b->sigma_on_device = true;
+  *out = b;
+  return PLSH_OK;
+}
+
 plsh_status plsh_bins_info(const plsh_bins* bins, int64_t* n, int32_t* H, int32_t* s,
                            int64_t* n_entries, void* stream) {
   if (bins == nullptr) return fail(PLSH_ERR_INVALID, "bins is NULL");

@@ -148,3 +148,8 @@ def test_backward_rejects_bad_arguments(lib):
     assert call(bad, k, k) == plsh.PLSH_ERR_INVALID        # dQ shape
     assert call(q, q, k) == plsh.PLSH_ERR_INVALID          # dK shape
     assert call(q, k, T(256, plsh.PLSH_F32, 1, 1, 128, 128)) == plsh.PLSH_ERR_INVALID
+
+
+def test_share_groups_rejects_null(lib):
+    out = ctypes.c_void_p()
+    assert lib.plsh_bins_share_groups(None, 4, None, ctypes.byref(out)) == plsh.PLSH_ERR_INVALID
