@@ -1,7 +1,6 @@
-"""GPU checks of plsh_alibi_attn_backward against the oracle's gradients,
-written for the GB300 run that first verifies the entry point (rename to
-test_*.py then).  fp32 inputs: 1e-4 relative to the largest gradient entry;
-bf16 inputs: the gradients are rounded to bf16, 1e-2 of that scale."""
+"""GPU checks of plsh_alibi_attn_backward against the oracle's gradients.
+fp32 inputs: 1e-4 relative to the largest gradient entry; bf16 inputs: the
+gradients are rounded to bf16, 1e-2 of that scale."""
 import numpy as np
 import pytest
 import torch

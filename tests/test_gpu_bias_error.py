@@ -1,8 +1,7 @@
-"""GPU checks of plsh_bias_error against the oracle, written for the GB300 run
-that first verifies the entry point (rename to test_*.py then): the exact
-max-norm error and the Lanczos spectral estimate against the dense fp64
-oracle on small n, the closed forms of all-singleton bins, and the
-O(1/sqrt(s)) decay at n = 16384."""
+"""GPU checks of plsh_bias_error against the oracle: the exact max-norm error
+and the Lanczos spectral estimate against the dense fp64 oracle on small n,
+the closed forms of all-singleton bins, and the O(1/sqrt(s)) decay at
+n = 16384."""
 import math
 
 import numpy as np

@@ -1,5 +1,4 @@
-"""GPU checks of plsh_bins_share_groups, for the GB300 run that first
-verifies it (rename to test_*.py then): exact start lists and draws against
+"""GPU checks of plsh_bins_share_groups: exact start lists and draws against
 the oracle, and attention on shared hashes against the oracle rows."""
 import numpy as np
 import pytest
