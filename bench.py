@@ -57,7 +57,7 @@ def work_counts(w, offsets, starts):
     causal else b^2 (QK^T and PV per (i, j) pair in a block); bytes = Q, K, V
     read once and O written once.  Also the tensor-core work the kernel
     executes: per (b, h, 128-row tile) every key tile of the union envelope,
-    three 128x128x128 products (S, P_hi V, P_lo V)."""
+    two 128x128x128 products (S in bf16, P V in f16)."""
     lens = np.diff(starts.astype(np.int64))
     # drop the terminal-to-next-hash differences: use per-hash slices
     pairs = 0
@@ -80,7 +80,7 @@ def work_counts(w, offsets, starts):
     f_block = 4.0 * w.d * w.B * pairs
     e = 2 if w.dtype == "bf16" else 4
     bytes_ = w.B * w.n * w.d * e * (2 * w.Hq + 2 * w.Hkv)
-    mma = w.B * env_tiles * 3 * 2.0 * 128 * 128 * 128
+    mma = w.B * env_tiles * 2 * 2.0 * 128 * 128 * 128
     return f_block, bytes_, mma, env_tiles * w.B
 
 

@@ -42,8 +42,14 @@ typedef enum {
   PLSH_ERR_CUDA = 2,         /* a CUDA runtime/driver call failed           */
   PLSH_ERR_NOMEM = 3,        /* device or host allocation failed            */
   PLSH_ERR_TIMEOUT = 4,      /* a device-side bounded wait ran out          */
-  PLSH_ERR_UNSUPPORTED = 5   /* valid request the library does not serve    */
+  PLSH_ERR_UNSUPPORTED = 5,  /* valid request the library does not serve    */
+  PLSH_ERR_RANGE = 6         /* an input value beyond the range the kernel
+                                computes in (V beyond +-65504 on the
+                                tensor-core path), found on the device      */
 } plsh_status;
+
+/* Which kernel serves an attention call (plsh_attn_path). */
+typedef enum { PLSH_PATH_CUDA_CORES = 0, PLSH_PATH_TENSOR_CORES = 1 } plsh_path;
 
 typedef enum { PLSH_F32 = 0, PLSH_BF16 = 1 } plsh_dtype;
 
@@ -108,8 +114,6 @@ plsh_status plsh_bins_from_host(int64_t n, int32_t H, int32_t s,
                                 const int64_t* offsets, const int32_t* starts,
                                 void* stream, plsh_bins** out);
 
-/* Shape of a handle.  n_entries (bins + terminals over all hashes) needs the
- * device contents: this call synchronises `stream` when n_entries != NULL. */
 /*
  * plsh_bins_fixed -- deterministic fixed blocks in place of random hashes (the
  * "fixed blocks" baseline of the summary's Mistral fine-tuning experiment,
@@ -180,6 +184,8 @@ plsh_status plsh_bias_error(const plsh_bins* bins, double sigma, int32_t h,
 plsh_status plsh_bins_share_groups(const plsh_bins* src, int32_t Hq, void* stream,
                                    plsh_bins** out);
 
+/* Shape of a handle.  n_entries (bins + terminals over all hashes) needs the
+ * device contents: this call synchronises `stream` when n_entries != NULL. */
 plsh_status plsh_bins_info(const plsh_bins* bins, int64_t* n, int32_t* H,
                            int32_t* s, int64_t* n_entries, void* stream);
 
@@ -209,11 +215,19 @@ void plsh_bins_free(plsh_bins* bins);
  * Computed as sum_j c_ij e^{S_ij} v_j / sum_j c_ij e^{S_ij}, with c_ij the
  * number of hashes that put i and j in one bin.
  *
- *   Q [B,Hq,n,d]; K, V [B,Hkv,n,d]; O [B,Hq,n,d], all the same dtype
- *   (PLSH_BF16: tcgen05 tensor-core path, d = 128; PLSH_F32 or d = 64: CUDA
- *   core path; fp32 accumulation and softmax in both).  Hq % Hkv == 0,
- *   bins->n == n, bins->H == Hq, d in {64, 128}.
+ *   Q [B,Hq,n,d]; K, V [B,Hkv,n,d]; O [B,Hq,n,d], all the same dtype,
+ *   Hq % Hkv == 0, bins->n == n, bins->H == Hq, d in {64, 128}.
  *   causal   non-zero: keys j <= i only.
+ * Kernels (plsh_attn_path tells which one a call takes, without launching):
+ *   tensor cores  bf16 with d = 128 and s within the kernel's shared memory
+ *                 (s <= 47 causal, s <= 27 without the mask): QK^T in
+ *                 bf16, the weights P and V in f16 for P V (every bf16
+ *                 value of V up to 65504 is an f16 value; P keeps 11
+ *                 significant bits), fp32 accumulation and softmax.  A value of V beyond +-65504 is reported by
+ *                 plsh_stream_status() as PLSH_ERR_RANGE (O is then not
+ *                 valid); T~ is linear in V, so V scaled down by a power of
+ *                 two gives O scaled down by the same power.
+ *   CUDA cores    everything else (fp32, d = 64, larger s): fp32 throughout.
  * Asynchronous on `stream`.  A device-side wait that runs out (a bug, never
  * expected) is reported by the next plsh_stream_status().
  */
@@ -237,20 +251,37 @@ plsh_status plsh_alibi_attn(const plsh_tensor* Q, const plsh_tensor* K,
  * allocation routine.
  *
  * Limits: bf16, d = 128, s within the tensor-core kernel's shared-memory
- * budget (s <= 40 causal), at most 1023 query heads and 65536 work items
- * (one item per two 128-row query tiles: B * Hq * ceil(n/128) / 2, e.g.
+ * budget (s <= 47 causal, s <= 27 without the mask), at most 1023 query
+ * heads and 65536 work items (one item per two 128-row query tiles:
+ * B * Hq * ceil(n/128) / 2, e.g.
  * n = 131072 with 40 heads uses 20480); larger requests return
  * PLSH_ERR_UNSUPPORTED and launch nothing.
  * The first call on each device resolves the array's device address
- * (cudaGetSymbolAddress); make that first call before any stream capture.
- * Every call on a device shares the one array and each call resets it before
- * use, so calls whose kernels overlap on the GPU (different streams without
- * ordering) race and must not be issued.  Device-side wait timeouts of this
- * path are recorded in the array, not reported by plsh_stream_status().
+ * (cudaGetSymbolAddress) and keeps it for the life of the device's primary
+ * context (a process that resets the device must not call this entry point
+ * again); make that first call before any stream capture.
+ * Every call on a device shares the one array and each call resets its work
+ * counters before use, so calls whose kernels overlap on the GPU (different
+ * streams without ordering) race and must not be issued.  A device-side wait
+ * that runs out (limit: plsh_set_wait_limit_ns) and a value of V beyond
+ * +-65504 are recorded in the array's error word, which persists across calls
+ * until plsh_noalloc_status() reads and clears it; plsh_stream_status() does
+ * not see them.
  */
 plsh_status plsh_alibi_attn_noalloc(const plsh_tensor* Q, const plsh_tensor* K,
                                     const plsh_tensor* V, const plsh_bins* bins,
                                     int32_t causal, plsh_tensor* O, void* stream);
+
+/*
+ * plsh_noalloc_status -- the error word of plsh_alibi_attn_noalloc on the
+ * current device.  Synchronises `stream`, reads the word from the fixed
+ * array (no allocation), clears it, and returns PLSH_ERR_TIMEOUT if a wait
+ * ran out, else PLSH_ERR_RANGE if a value of V was beyond +-65504, else
+ * PLSH_OK, covering every allocation-free call since the last report.  Call
+ * it once the calls it should cover are queued on `stream` (or on streams
+ * `stream` waits for).
+ */
+plsh_status plsh_noalloc_status(void* stream);
 
 /*
  * plsh_alibi_attn_host -- plsh_alibi_attn on tensors in host memory.  The
@@ -310,9 +341,19 @@ plsh_status plsh_alibi_decode(const plsh_tensor* q, const plsh_tensor* K,
                               plsh_tensor* o, void* stream);
 
 /* Synchronises `stream`, then reports CUDA errors and the library's device
- * error flag (PLSH_ERR_TIMEOUT when a bounded device wait ran out), clearing
- * the flag. */
+ * error flag, clearing the flag: PLSH_ERR_TIMEOUT when a bounded device wait
+ * ran out, else PLSH_ERR_RANGE when a tensor-core attention call met a value
+ * of V beyond +-65504. */
 plsh_status plsh_stream_status(void* stream);
+
+/*
+ * plsh_attn_path -- the kernel plsh_alibi_attn (bins != NULL) or
+ * plsh_alibi_exact (bins == NULL) takes for a query tensor of Q's shape and
+ * dtype, written to *path (a plsh_path).  Launches nothing, allocates
+ * nothing; PLSH_ERR_INVALID for a NULL Q or path.
+ */
+plsh_status plsh_attn_path(const plsh_tensor* Q, const plsh_bins* bins, int32_t causal,
+                           int32_t* path);
 
 /* Debug knob: limit in nanoseconds of every device-side wait launched after
  * this call on the current device (0 restores the default of 2 s). */

@@ -22,12 +22,13 @@ from . import build as _build_mod
 
 __all__ = ["build", "load", "sample_bins", "bins_from_host", "bins_fixed", "bins_share_groups", "Bins", "alibi_attn",
            "alibi_attn_noalloc", "alibi_attn_host",
-           "alibi_exact", "alibi_decode", "alibi_attn_backward", "bias_error", "stream_status", "set_wait_limit_ns", "PlshError",
-           "library_path"]
+           "alibi_exact", "alibi_decode", "alibi_attn_backward", "bias_error", "stream_status",
+           "noalloc_status", "attn_path", "set_wait_limit_ns", "PlshError", "library_path"]
 
 PLSH_OK, PLSH_ERR_INVALID, PLSH_ERR_CUDA, PLSH_ERR_NOMEM, PLSH_ERR_TIMEOUT, \
-    PLSH_ERR_UNSUPPORTED = range(6)
+    PLSH_ERR_UNSUPPORTED, PLSH_ERR_RANGE = range(7)
 PLSH_F32, PLSH_BF16 = 0, 1
+PLSH_PATH_CUDA_CORES, PLSH_PATH_TENSOR_CORES = 0, 1
 
 _lock = threading.Lock()
 _lib = None
@@ -88,6 +89,8 @@ def load():
             "plsh_alibi_exact": [TP, TP, TP, D, I32, TP, P],
             "plsh_alibi_decode": [TP, TP, TP, P, I64, TP, P],
             "plsh_stream_status": [P],
+            "plsh_noalloc_status": [P],
+            "plsh_attn_path": [TP, P, I32, ctypes.POINTER(I32)],
             "plsh_set_wait_limit_ns": [U64],
         }
         for name, args in sig.items():
@@ -335,6 +338,22 @@ def bias_error(bins: Bins, sigma: float, h: int, lanczos_iters: int = 60, seed: 
 def stream_status(stream=None):
     """plsh_stream_status: synchronise and raise on device-side errors."""
     _check(load().plsh_stream_status(_stream(stream)))
+
+
+def noalloc_status(stream=None):
+    """plsh_noalloc_status: synchronise and raise on the error word of the
+    allocation-free entry point (timeouts, V out of f16 range)."""
+    _check(load().plsh_noalloc_status(_stream(stream)))
+
+
+def attn_path(Q, bins=None, causal: bool = True) -> str:
+    """plsh_attn_path: "tensor_cores" or "cuda_cores", the kernel that
+    alibi_attn (bins given) or alibi_exact (bins None) takes for Q."""
+    t = _desc(Q)
+    out = ctypes.c_int32()
+    _check(load().plsh_attn_path(ctypes.byref(t), bins.handle if bins is not None else None,
+                                 int(bool(causal)), ctypes.byref(out)))
+    return "tensor_cores" if out.value == PLSH_PATH_TENSOR_CORES else "cuda_cores"
 
 
 def set_wait_limit_ns(ns: int):

@@ -6,6 +6,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 #include <numeric>
 #include <string>
@@ -325,6 +326,23 @@ plsh_status item_table(plsh::DeviceCtx* ctx, int B, int Hq, int Hkv, int qt0, in
 
 enum class Path { Auto, Simt, Tc };
 
+// The tensor-core kernel serves bf16 with d = 128 and s within its shared
+// memory; everything else takes the CUDA-core kernel.
+bool tc_path_ok(int dtype, int64_t d, int s, int causal, int exact) {
+  return dtype == PLSH_BF16 && d == 128 &&
+         plsh::attn_tc_smem_bytes(s, causal, exact) <= 232448;
+}
+
+// Status of the device error word: bit 0 a bounded wait ran out, bit 1 a
+// value of V beyond f16's range on the tensor-core path.
+plsh_status device_flag_status(int flag) {
+  if (flag & 1) return fail(PLSH_ERR_TIMEOUT, "a device-side wait ran out of time");
+  if (flag & 2)
+    return fail(PLSH_ERR_RANGE, "V holds a value beyond +-65504, which the tensor-core path "
+                                "takes in f16 (scale V down by a power of two: O scales with it)");
+  return PLSH_OK;
+}
+
 Path path_override() {
   const char* p = getenv("PLSH_PATH");
   if (p == nullptr) return Path::Auto;
@@ -364,8 +382,7 @@ plsh_status run_attention(const plsh_tensor* Q, const plsh_tensor* K, const plsh
     std::lock_guard<std::mutex> lk(g_ctx_mu);
     a.queue = ctx->d_queue + 2 * (ctx->slot_counter++ % plsh::kQueueSlots);
   }
-  const bool tc_ok = Q->dtype == PLSH_BF16 && Q->d == 128 &&
-                     plsh::attn_tc_smem_bytes(a.s, a.causal, a.exact) <= 232448;
+  const bool tc_ok = tc_path_ok(Q->dtype, Q->d, a.s, a.causal, a.exact);
   Path path = path_override();
   if (path == Path::Auto) path = tc_ok ? Path::Tc : Path::Simt;
   if (path == Path::Tc && !tc_ok)
@@ -401,35 +418,50 @@ std::mutex g_noalloc_mu;
 
 constexpr int kNoAllocMaxUnits = 512;
 
+// Wait limit of the allocation-free path per device (set with
+// plsh_set_wait_limit_ns; kept apart from the per-device context, whose
+// creation allocates).
+std::atomic<uint64_t> g_noalloc_wait_ns[kMaxDevices];
+
 // Work units in cost order: a pair of heads of one KV group (every row tile
 // is an item), or the last head of an odd group (pairs of its row tiles).
+// Consecutive units of equal cost form a run whose items interleave.
 struct NoAllocUnits {
   int count;
-  int unit[kNoAllocMaxUnits];   // hA | hB << 10 | leftover << 20
+  int unit[kNoAllocMaxUnits];   // hA | hB << 10 | leftover << 20 | run start << 21
 };
 
 // One thread per work item: writes the item table the tensor-core kernel
-// reads, in unit order, batch-major inside a unit; thread 0 also clears the
-// queue counters and the error flag.
+// reads, in the order of the ordinary entry point's table: runs in cost
+// order; inside a run, row tiles from the last (the most keys under the
+// causal mask) down, then batch elements, then units.  Thread 0 also clears
+// the queue counters (not the error word, which persists until read).
 __global__ void noalloc_items_kernel(int4* scratch, const __grid_constant__ NoAllocUnits u,
                                      int B, int QT, int num_items) {
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx == 0) scratch[0] = make_int4(0, 0, 0, 0);
+  if (idx == 0) {
+    reinterpret_cast<int*>(scratch)[0] = 0;
+    reinterpret_cast<int*>(scratch)[1] = 0;
+  }
   if (idx >= num_items) return;
   int off = idx;
-  for (int k = 0; k < u.count; ++k) {
-    const int code = u.unit[k];
-    const bool leftover = (code >> 20) & 1;
-    const int per_b = leftover ? (QT + 1) / 2 : QT;
-    if (off < B * per_b) {
-      const int b = off / per_b, q = off % per_b;
+  for (int k = 0; k < u.count;) {
+    int R = 1;
+    while (k + R < u.count && !((u.unit[k + R] >> 21) & 1)) ++R;
+    const bool leftover = (u.unit[k] >> 20) & 1;
+    const int levels = leftover ? (QT + 1) / 2 : QT;
+    if (off < R * B * levels) {
+      const int lvl = off / (R * B), rem = off % (R * B);
+      const int b = rem / R, code = u.unit[k + rem % R];
+      const int q = levels - 1 - lvl;
       const int hA = code & 1023, hB = (code >> 10) & 1023;
       const int qtA = leftover ? 2 * q : q;
       const int qtB = leftover ? (2 * q + 1 < QT ? 2 * q + 1 : -1) : q;
       scratch[1 + idx] = make_int4(b, hA | (hB << 16), qtA, qtB);
       return;
     }
-    off -= B * per_b;
+    off -= R * B * levels;
+    k += R;
   }
 }
 
@@ -773,8 +805,8 @@ plsh_status plsh_alibi_attn_host(const plsh_tensor* Q, const plsh_tensor* K,
   // otherwise): the copies of chunk c + 1 in and chunk c - 1 out overlap the
   // kernel on chunk c; without the causal mask every chunk needs all keys
   const int QT = (int)((n + 127) / 128);
-  const bool tc = Q->dtype == PLSH_BF16 && Q->d == 128 && path_override() != Path::Simt &&
-                  plsh::attn_tc_smem_bytes(bins->s, causal ? 1 : 0, 0) <= 232448;
+  const bool tc = tc_path_ok(Q->dtype, Q->d, bins->s, causal ? 1 : 0, 0) &&
+                  path_override() != Path::Simt;
   const int nchunk = tc ? std::min(plsh::kMaxHostChunks, QT) : 1;
   const int tpc = (QT + nchunk - 1) / nchunk;
   const bool kv_chunked = causal && nchunk > 1;
@@ -913,9 +945,8 @@ plsh_status plsh_stream_status(void* stream) {
   if (flag != 0) {
     PLSH_TRY_CUDA(cudaMemset(ctx->d_err, 0, sizeof(int)), "clear error flag");
     PLSH_TRY_CUDA(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
-    return fail(PLSH_ERR_TIMEOUT, "a device-side wait ran out of time");
   }
-  return PLSH_OK;
+  return device_flag_status(flag);
 }
 
 plsh_status plsh_set_wait_limit_ns(uint64_t ns) {
@@ -923,6 +954,7 @@ plsh_status plsh_set_wait_limit_ns(uint64_t ns) {
   plsh_status st = current_ctx(&ctx);
   if (st != PLSH_OK) return st;
   ctx->wait_ns = ns == 0 ? plsh::kDefaultWaitNs : ns;
+  g_noalloc_wait_ns[ctx->device].store(ctx->wait_ns, std::memory_order_relaxed);
   return PLSH_OK;
 }
 
@@ -934,6 +966,7 @@ const char* plsh_status_string(plsh_status status) {
     case PLSH_ERR_NOMEM: return "out of memory";
     case PLSH_ERR_TIMEOUT: return "device wait timed out";
     case PLSH_ERR_UNSUPPORTED: return "unsupported";
+    case PLSH_ERR_RANGE: return "input value out of range";
   }
   return "unknown status";
 }
@@ -950,8 +983,7 @@ plsh_status plsh_alibi_attn_noalloc(const plsh_tensor* Q, const plsh_tensor* K,
   if (bins->n != Q->n) return fail(PLSH_ERR_INVALID, "bins were drawn for another n");
   if (bins->H != Q->H) return fail(PLSH_ERR_INVALID, "bins were drawn for another number of heads");
   if ((st = check_bins_device(bins)) != PLSH_OK) return st;
-  if (Q->dtype != PLSH_BF16 || Q->d != 128 ||
-      plsh::attn_tc_smem_bytes(bins->s, causal ? 1 : 0, 0) > 232448)
+  if (!tc_path_ok(Q->dtype, Q->d, bins->s, causal ? 1 : 0, 0))
     return fail(PLSH_ERR_UNSUPPORTED, "allocation-free path: needs bf16, d = 128 and s within "
                                       "the tensor-core kernel's shared-memory budget");
   const int B = (int)Q->B, Hq = (int)Q->H, Hkv = (int)K->H;
@@ -1002,6 +1034,9 @@ plsh_status plsh_alibi_attn_noalloc(const plsh_tensor* Q, const plsh_tensor* K,
     u.unit[b2] = cu;
     key[b2] = ck;
   }
+  for (int a = 0; a < u.count; ++a)        // runs of equal cost and unit kind
+    if (a == 0 || key[a] != key[a - 1] || ((u.unit[a] ^ u.unit[a - 1]) >> 20 & 1))
+      u.unit[a] |= 1 << 21;
   if (num_items > kNoAllocMaxItems)
     return fail(PLSH_ERR_UNSUPPORTED,
                 "allocation-free path: " + std::to_string(num_items) + " work items exceed its " +
@@ -1048,8 +1083,42 @@ plsh_status plsh_alibi_attn_noalloc(const plsh_tensor* Q, const plsh_tensor* K,
   a.num_items = (int)num_items;
   a.queue = reinterpret_cast<int*>(scratch);
   a.err = reinterpret_cast<int*>(scratch) + 2;
-  a.wait_ns = plsh::kDefaultWaitNs;
+  const uint64_t wl = g_noalloc_wait_ns[dev].load(std::memory_order_relaxed);
+  a.wait_ns = wl == 0 ? plsh::kDefaultWaitNs : wl;
+  a.stall = fault_is("stall") ? 1 : 0;
   PLSH_TRY_CUDA(plsh::launch_attn_tc(a, nullptr, sms, cs), "attention launch");
+  return PLSH_OK;
+}
+
+plsh_status plsh_noalloc_status(void* stream) {
+  int dev = -1;
+  PLSH_TRY_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(PLSH_ERR_UNSUPPORTED, "device index out of range");
+  cudaStream_t cs = (cudaStream_t)stream;
+  PLSH_TRY_CUDA(cudaStreamSynchronize(cs), "cudaStreamSynchronize");
+  PLSH_TRY_CUDA(cudaGetLastError(), "pending CUDA error");
+  // the error word is the third int of the array's first element
+  int word = 0;
+  const size_t at = 2 * sizeof(int);
+  PLSH_TRY_CUDA(cudaMemcpyFromSymbolAsync(&word, g_noalloc_scratch, sizeof(int), at,
+                                          cudaMemcpyDeviceToHost, cs), "read error word");
+  PLSH_TRY_CUDA(cudaStreamSynchronize(cs), "cudaStreamSynchronize");
+  if (word != 0) {
+    const int zero = 0;
+    PLSH_TRY_CUDA(cudaMemcpyToSymbolAsync(g_noalloc_scratch, &zero, sizeof(int), at,
+                                          cudaMemcpyHostToDevice, cs), "clear error word");
+    PLSH_TRY_CUDA(cudaStreamSynchronize(cs), "cudaStreamSynchronize");
+  }
+  return device_flag_status(word);
+}
+
+plsh_status plsh_attn_path(const plsh_tensor* Q, const plsh_bins* bins, int32_t causal,
+                           int32_t* path) {
+  if (Q == nullptr || path == nullptr) return fail(PLSH_ERR_INVALID, "NULL argument");
+  *path = tc_path_ok(Q->dtype, Q->d, bins ? bins->s : 0, causal ? 1 : 0, bins ? 0 : 1) &&
+                  path_override() != Path::Simt
+              ? PLSH_PATH_TENSOR_CORES
+              : PLSH_PATH_CUDA_CORES;
   return PLSH_OK;
 }
 

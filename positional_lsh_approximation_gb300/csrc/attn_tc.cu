@@ -21,7 +21,7 @@
 // Exact ALiBi (the dense comparator) runs on the same pipeline with weight
 // e^{S_ij - |i-j|/sigma_h} over every key tile.
 //
-// One persistent CTA per SM, 11 warps, two 128-row query tiles A and B per
+// One persistent CTA per SM, 12 warps, two 128-row query tiles A and B per
 // work item (two heads of one KV group at the same rows, or two row tiles of
 // one head), sharing every K/V tile:
 //   warp 10     scheduler: pops items from a global queue (cost order),
@@ -30,6 +30,9 @@
 //   warp 8      producer: TMA-loads the item's first K tile, then Q_A and
 //               Q_B, then the other K/V tiles from the diagonal tile down
 //               (a ring of three 32 KB slots);
+//   warp 11     converter: turns each V tile from bf16 into f16 in place in
+//               shared memory once it lands (exact within f16's range; a
+//               value beyond it raises the range bit of the error flag);
 //   warp 9      one thread issues tcgen05.mma in one stream across items,
 //               PV_A(g-1) S_A(g) PV_B(g-1) S_B(g) ..., so that while one
 //               warpgroup turns its scores into weights the tensor core works
@@ -39,17 +42,19 @@
 //   warps 0-3   softmax of tile A, warps 4-7 softmax of tile B: one thread
 //               per row, tcgen05.ld of the score row, running max over the
 //               valid keys, lazy rescale of O in TMEM (only when the max grows
-//               by more than 2^8), P = c 2^(x - m) split into two bf16 terms
-//               P_hi + P_lo (truncated head, rounded remainder) written back
-//               over the consumed score columns, fp32 row sums, and the O / l
-//               epilogue (through shared memory into whole-line stores).
-//   O += P_hi V + P_lo V runs as two tensor-core products with A read from
-//   TMEM: a single bf16 P carries a 2^-9 relative error per weight, which
-//   shows in rows whose few keys cancel; the pair carries about 2^-16.
+//               by more than 2^8), P = c 2^(x - m) rounded to f16 and
+//               written back over score columns already consumed, fp32 row
+//               sums, and the O / l epilogue (through shared memory into
+//               whole-line stores).
+//   O += P V runs on the tensor cores in f16 with A read from TMEM: f16 keeps
+//   11 significant bits of each weight (bf16 only 8, whose 2^-9 relative
+//   error per weight shows in rows whose few keys cancel), and every bf16
+//   value of V within f16's range is an f16 value.
 // TMEM columns: S_A | S_B | O_A | O_B.  Every wait on an mbarrier is bounded;
 // on expiry the CTA raises the library error flag, drains its in-flight copies
 // and MMAs, frees TMEM and exits.
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <limits.h>
 #include <stdint.h>
@@ -68,11 +73,12 @@ using namespace ptx;
 constexpr int BM = 128;      // query rows per tile (MMA M)
 constexpr int BN = 128;      // keys per tile (MMA N of QK^T, K of PV)
 constexpr int HD = 128;      // head dim (MMA K of QK^T, N of PV)
-constexpr int kWarps = 11;
+constexpr int kWarps = 12;
 constexpr int kThreads = kWarps * 32;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kSchedWarp = 10;
+constexpr int kConvWarp = 11;
 constexpr int kRing = 3;                         // work items in flight
 constexpr int kSlots = 3;                        // K/V tile ring depth
 constexpr int kMaxSlots = 4;                     // barriers reserved for the ring
@@ -81,9 +87,10 @@ constexpr uint32_t kHalfBytes = kTileBytes / 2;  // one 64-column TMA box
 constexpr uint32_t OFF_Q = 0;                          // Q_A, Q_B
 constexpr uint32_t OFF_KV = OFF_Q + 2 * kTileBytes;    // ring of `slots` tiles
 constexpr uint32_t kTmemCols = 512;   // S_A | S_B | O_A | O_B; P over S
+constexpr uint32_t kColP = 64;        // P (f16 pairs) in the upper half of S
 constexpr uint32_t kColO = 256;
 constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (factor 256)
-constexpr float kGrowLog2 = 24.0f;    // largest weight 2^24 c before a mid-tile rescale
+constexpr float kGrowLog2 = 15.0f;    // largest weight 2^15 before a mid-tile rescale (f16 P)
 constexpr unsigned FULL = 0xffffffffu;
 constexpr int kWordsPerTile = BM / 32;
 constexpr uint32_t kOutBytes = 8 * 32 * 64 * 2;   // O transpose: 32 rows x 64 bf16 per warp
@@ -93,8 +100,13 @@ enum {
   B_KVEMPTY = B_KVFULL_END, B_KVEMPTY_END = B_KVEMPTY + kMaxSlots,
   B_SFULL = B_KVEMPTY_END, B_SFULL1, B_PFULL, B_PFULL1, B_ODONE, B_ODONE1,
   B_IFULL, B_IFULL_END = B_IFULL + kRing, B_IEMPTY = B_IFULL_END,
-  B_IEMPTY_END = B_IEMPTY + kRing, B_DRAIN = B_IEMPTY_END, NUM_BARS
+  B_IEMPTY_END = B_IEMPTY + kRing, B_DRAIN = B_IEMPTY_END,
+  B_VREADY, B_VREADY_END = B_VREADY + kMaxSlots, NUM_BARS
 };
+
+// Error flag bits: 1 a wait ran out, 2 a value of V lies beyond f16's range.
+constexpr int kErrTimeout = 1;
+constexpr int kErrRange = 2;
 
 struct Item {
   int valid, b, hA, hB, qtA, qtB, kt_lo, kt_hi;
@@ -265,6 +277,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
     for (int k = 0; k < kMaxSlots; ++k) {
       mbar_init(bar(B_KVFULL + k), 1);
       mbar_init(bar(B_KVEMPTY + k), 1);
+      mbar_init(bar(B_VREADY + k), 1);
     }
     for (int k = 0; k < 2; ++k) {
       mbar_init(bar(B_SFULL + k), 1);
@@ -273,8 +286,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
     }
     for (int k = 0; k < kRing; ++k) {
       mbar_init(bar(B_IFULL + k), 1);
-      // released by the producer, the MMA thread and every softmax thread
-      mbar_init(bar(B_IEMPTY + k), 2 + 2 * BM);
+      // released by the producer, the converter, the MMA thread and every
+      // softmax thread
+      mbar_init(bar(B_IEMPTY + k), 3 + 2 * BM);
     }
     mbar_init(bar(B_DRAIN), 1);
     ctl->abort = 0;
@@ -394,7 +408,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
     }
     if (!ok && lane == 0) {
       *abort = 1;
-      atomicOr(a.err, 1);
+      atomicOr(a.err, kErrTimeout);
     }
     __syncwarp();
   } else if (warp == kProducerWarp) {
@@ -447,7 +461,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       }
       if (!ok) {
         *abort = 1;
-        atomicOr(a.err, 1);
+        atomicOr(a.err, kErrTimeout);
       }
       // let every copy this warp started land before the CTA can exit
       if (q_issued) {
@@ -459,16 +473,78 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
           mbar_wait(bar(B_KVFULL + sl), (uint32_t)(kv_issued[sl] - 1) & 1u, nullptr, lim);
     }
     __syncwarp();
+  } else if (warp == kConvWarp) {
+    // ----------------------------------------------------------- converter
+    // follows the producer's load order (per item, tiles from the diagonal
+    // down, K then V) and turns every V tile into f16 in place: the element
+    // positions of the swizzled layout do not depend on the element type
+    bool ok = true;
+    int ld = 0;
+    float vmax = 0.f;                   // largest |v| seen, as f32
+    for (int seq = 0; ok; ++seq) {
+      const int slot = seq % kRing;
+      const uint32_t use = (uint32_t)(seq / kRing);
+      ok = __all_sync(FULL, mbar_wait(bar(B_IFULL + slot), use & 1u, abort, lim));
+      if (!ok) break;
+      const Item it = read_item(ctl, slot);
+      if (!it.valid) break;
+      for (int kt = it.kt_hi - 1; kt >= it.kt_lo; --kt, ld += 2) {
+        const int lv = ld + 1;
+        const uint32_t sl = (uint32_t)lv % nslots;
+        ok = __all_sync(FULL, mbar_wait(bar(B_KVFULL + sl), ((uint32_t)lv / nslots) & 1u, abort,
+                                        lim));
+        if (!ok) break;
+        const uint32_t vb = sbase + OFF_KV + sl * kTileBytes + (uint32_t)lane * 16u;
+#pragma unroll 4
+        for (uint32_t c = 0; c < kTileBytes / 16u; c += 32) {
+          const uint4 v = ld_shared_v4(vb + c * 16u);
+          const float a0 = __uint_as_float(v.x << 16), a1 = __uint_as_float(v.x & 0xffff0000u);
+          const float b0 = __uint_as_float(v.y << 16), b1 = __uint_as_float(v.y & 0xffff0000u);
+          const float c0 = __uint_as_float(v.z << 16), c1 = __uint_as_float(v.z & 0xffff0000u);
+          const float d0 = __uint_as_float(v.w << 16), d1 = __uint_as_float(v.w & 0xffff0000u);
+          vmax = max3(vmax, fabsf(a0), fabsf(a1));
+          vmax = max3(vmax, fabsf(b0), fabsf(b1));
+          vmax = max3(vmax, fabsf(c0), fabsf(c1));
+          vmax = max3(vmax, fabsf(d0), fabsf(d1));
+          st_shared_v4(vb + c * 16u, pack_f16(a0, a1), pack_f16(b0, b1), pack_f16(c0, c1),
+                       pack_f16(d0, d1));
+        }
+        // the tensor core reads the tile through the async proxy
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_VREADY + sl));
+      }
+      if (!ok) break;
+      if (lane == 0) mbar_arrive(bar(B_IEMPTY + slot));
+      __syncwarp();
+    }
+    // 65520 and above round to infinity in f16 (NaN inputs stay NaN)
+    const bool range = __any_sync(FULL, vmax >= 65520.f);
+    if (lane == 0) {
+      if (!ok) {
+        *abort = 1;
+        atomicOr(a.err, kErrTimeout);
+      }
+      if (range) atomicOr(a.err, kErrRange);
+    }
+    __syncwarp();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, 0, 0);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, HD, 0, 1);
+      constexpr uint32_t idesc_pv = idesc_f16_f32(BM, HD, 0, 1);
       bool ok = true;
       int ld = 0;        // K/V loads consumed so far (same numbering as producer)
       int gt = 0;        // tiles processed so far (both tiles advance together)
       auto wait_slot = [&](int l) -> bool {
         return mbar_wait(bar(B_KVFULL + (uint32_t)l % nslots), ((uint32_t)l / nslots) & 1u, abort,
+                        lim);
+      };
+      // V load l (odd) sits in slot l % 3; that slot holds V on every other
+      // use, so this is its (l / 6)-th V: the converter's phase
+      static_assert(kSlots == 3, "V phases assume a ring of three slots");
+      auto wait_v = [&](int l) -> bool {
+        return mbar_wait(bar(B_VREADY + (uint32_t)l % nslots), ((uint32_t)l / 6u) & 1u, abort,
                         lim);
       };
       // descriptors of the tiles' first 16-column slices; a slice further
@@ -489,16 +565,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       };
       auto issue_pv = [&](int tile, int lv, bool first) {
         const uint64_t vd = desc_add(dv0, ((uint32_t)lv % nslots) * (kTileBytes >> 4));
-        // keys 16kk..16kk+15 sit in chunk kk/2: P_hi in its first 16
-        // columns, P_lo in the next 16, 8 packed columns per 16 keys
-        const uint32_t pcol = tmem + tile * BN;
+        // keys 16kk..16kk+15: 8 columns of f16 pairs at 8 kk past the
+        // tile's P base
+        const uint32_t pcol = tmem + tile * BN + kColP;
         const uint32_t ocol = tmem + kColO + tile * HD;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
           const uint64_t bd = desc_add(vd, kk * (2048 >> 4));
-          const uint32_t ac = pcol + (kk >> 1) * 32 + (kk & 1) * 8;
-          mma_bf16_ts(ocol, ac, bd, idesc_pv, (first && kk == 0) ? 0u : 1u);
-          mma_bf16_ts(ocol, ac + 16, bd, idesc_pv, 1u);
+          mma_f16kind_ts(ocol, pcol + kk * 8, bd, idesc_pv, (first && kk == 0) ? 0u : 1u);
         }
       };
       // one continuous stream of tiles across items: the head of an item
@@ -515,7 +589,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         const int lk = ld;                      // K of this tile; V is ld + 1
         if (have_prev) {
           ok = mbar_wait(bar(B_PFULL + 0), (uint32_t)(gt - 1) & 1u, abort, lim) &&
-               wait_slot(prev_lv);
+               wait_v(prev_lv);
           if (!ok) break;
           tc_fence_after();
           issue_pv(0, prev_lv, prev_first);
@@ -568,7 +642,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       if (ok && have_prev) {
         // tail of the last tile
         ok = mbar_wait(bar(B_PFULL + 0), (uint32_t)(gt - 1) & 1u, abort, lim) &&
-             wait_slot(prev_lv);
+             wait_v(prev_lv);
         if (ok) {
           tc_fence_after();
           issue_pv(0, prev_lv, prev_first);
@@ -585,7 +659,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       }
       if (!ok) {
         *abort = 1;
-        atomicOr(a.err, 1);
+        atomicOr(a.err, kErrTimeout);
       }
       // every MMA issued by this thread has completed once this arrives
       mma_commit(bar(B_DRAIN));
@@ -870,9 +944,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
           }
         }
 
-        // pass 2: P = c 2^(x - m) = P_hi + P_lo (two bf16 terms) written over
-        // the chunk's own score columns; chunks in descending key order so
-        // that the breakpoint pointers only move down
+        // pass 2: P = c 2^(x - m) in f16 pairs, written over score columns
+        // already consumed; chunks in descending key order so that the
+        // breakpoint pointers only move down
         uint64_t lsum2 = f2_pack(0.f, 0.f);
 #pragma unroll 1
         for (int q = 3; q >= 0; --q) {
@@ -888,8 +962,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
               // no key of the chunk takes part in a row of this warp
               const uint32_t z[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u,
                                       0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-              tmem_st16(s_col + q * 32, z);
-              tmem_st16(s_col + q * 32 + 16, z);
+              tmem_st16(s_col + kColP + q * 16, z);
               continue;
             }
             tmem_ld32(s_col + q * 32, rr);
@@ -1002,7 +1075,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
             }
           }
           tmem_wait_ld();
-          uint32_t hi[16], lo[16];
+          uint32_t pk[16];
           {
             const bool all_flat = EXACT || __all_sync(FULL, flat);
             const float lgb = (!EXACT && all_flat) ? lg2((float)max(base, 1)) : 0.f;
@@ -1035,8 +1108,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
             if (one_pass) {
               // the chunk's largest exponent: far above the running max (a
               // jump of the scores), O, l and the chunks of this tile written
-              // so far are scaled down to the new max first (by a power of
-              // two: exact in fp32 and in both bf16 terms)
+              // so far are scaled down to the new max first, so that no
+              // weight passes 2^15 (f16 holds up to 65504)
               float c0 = -INFINITY, c1 = -INFINITY;
 #pragma unroll
               for (int e = 0; e < 32; e += 4) {
@@ -1064,14 +1137,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                 }
 #pragma unroll 1
                 for (int q3 = 3; q3 > q; --q3) {
-                  uint32_t w[32];
-                  tmem_ld32(s_col + q3 * 32, w);
+                  uint32_t w[16];
+                  tmem_ld16(s_col + kColP + q3 * 16, w);
                   tmem_wait_ld();
 #pragma unroll
-                  for (int e = 0; e < 32; ++e)
-                    w[e] = pack_bf16(__uint_as_float(w[e] << 16) * f,
-                                     __uint_as_float(w[e] & 0xffff0000u) * f);
-                  tmem_st32(s_col + q3 * 32, w);
+                  for (int e = 0; e < 16; ++e) {
+                    const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+                    w[e] = pack_f16(x.x * f, x.y * f);
+                  }
+                  tmem_st16(s_col + kColP + q3 * 16, w);
                 }
               }
             }
@@ -1111,23 +1185,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                 scale_by_planes<2, CAUSAL>(pv, base, up, dn);
               }
             }
-            // P_hi: the upper 16 bits of each weight (truncation, so that
-            // P - P_hi is exact in fp32); P_lo: that remainder rounded to
-            // bf16, relative error below 2^-16 for the pair
+            // P rounded to f16 pairs; the row sum takes the fp32 values
 #pragma unroll
             for (int e2 = 0; e2 < 16; ++e2) {
-              const uint64_t p2 = f2_pack(pv[2 * e2], pv[2 * e2 + 1]);
-              lsum2 = f2_add(lsum2, p2);
-              const uint32_t b0 = __float_as_uint(pv[2 * e2]), b1 = __float_as_uint(pv[2 * e2 + 1]);
-              float l0, l1;
-              f2_unpack(f2_sub(p2, f2_pack(__uint_as_float(b0 & 0xffff0000u),
-                                           __uint_as_float(b1 & 0xffff0000u))), l0, l1);
-              hi[e2] = __byte_perm(b0, b1, 0x7632);
-              lo[e2] = pack_bf16(l0, l1);
+              lsum2 = f2_add(lsum2, f2_pack(pv[2 * e2], pv[2 * e2 + 1]));
+              pk[e2] = pack_f16(pv[2 * e2], pv[2 * e2 + 1]);
             }
           }
-          tmem_st16(s_col + q * 32, hi);
-          tmem_st16(s_col + q * 32 + 16, lo);
+          // chunks run in descending order, so P of chunk q lands on the
+          // score columns of chunks q + 2 and q + 3, already consumed
+          tmem_st16(s_col + kColP + q * 16, pk);
         }
         float ls0, ls1;
         f2_unpack(lsum2, ls0, ls1);
@@ -1150,7 +1217,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
     }
     if (!ok && lane == 0) {
       *abort = 1;
-      atomicOr(a.err, 1);
+      atomicOr(a.err, kErrTimeout);
     }
   }
 

@@ -39,8 +39,9 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for st in range(6):
+    for st in range(7):
         assert lib.plsh_status_string(st)
+    assert lib.plsh_status_string(plsh.PLSH_ERR_RANGE) != lib.plsh_status_string(99)
     assert lib.plsh_last_error() is not None
 
 
@@ -153,3 +154,20 @@ def test_backward_rejects_bad_arguments(lib):
 def test_share_groups_rejects_null(lib):
     out = ctypes.c_void_p()
     assert lib.plsh_bins_share_groups(None, 4, None, ctypes.byref(out)) == plsh.PLSH_ERR_INVALID
+
+
+def test_attn_path_query(lib):
+    """plsh_attn_path names the kernel a call would take, launching nothing."""
+    T = plsh._Tensor
+    out = ctypes.c_int32(-1)
+
+    def path(dtype, d, bins=None, causal=1):
+        q = T(256, dtype, 1, 4, 1024, d)
+        st = lib.plsh_attn_path(ctypes.byref(q), bins, causal, ctypes.byref(out))
+        assert st == plsh.PLSH_OK
+        return out.value
+
+    assert path(plsh.PLSH_BF16, 128) == plsh.PLSH_PATH_TENSOR_CORES      # exact ALiBi
+    assert path(plsh.PLSH_BF16, 64) == plsh.PLSH_PATH_CUDA_CORES
+    assert path(plsh.PLSH_F32, 128) == plsh.PLSH_PATH_CUDA_CORES
+    assert lib.plsh_attn_path(None, None, 1, ctypes.byref(out)) == plsh.PLSH_ERR_INVALID

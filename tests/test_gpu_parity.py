@@ -1,7 +1,7 @@
 """CUDA path vs the fp64 oracle, through the C ABI.
 
 Tolerances (elementwise |gpu - oracle| <= atol + rtol |oracle|):
-  bf16 inputs: atol 2e-3, rtol 1e-2   (P and O are rounded to bf16)
+  bf16 inputs: atol 2e-3, rtol 1e-2   (P is rounded to f16, O to bf16)
   fp32 inputs: atol 1e-5, rtol 1e-5
 Bin boundaries and draws: bit-exact.
 """
@@ -272,3 +272,66 @@ def test_exact_full_size_sampled_rows(name):
         rows, _ = sample_rows(w, per_head=4 if name == "scout" else 12)
     ref = oracle.alibi_exact_rows(Q, K, V, sigma, w.causal, rows)
     assert_close(gather_rows(O, rows), ref, w.dtype, "exact " + name)
+
+
+# ------------------------------------------------ f16 weights and values
+def test_v_scaled_by_powers_of_two():
+    """P V runs in f16 on the tensor cores.  V scaled by 2^12 (values up to
+    about 2e4, every one an f16 value) gives O scaled by exactly 2^12, for the
+    approximation and for exact ALiBi; V scaled by 2^-16 (mostly f16
+    subnormals, rounded within 2^-25) stays within the scaled tolerance plus
+    one subnormal step of the oracle."""
+    n, s = 600, 8
+    w = Workload("vscale", 1, 4, 2, n, 128, "bf16", True, s, (1.5, 7.0, 40.0, 300.0),
+                 qkv_seed=17)
+    Q, K, V = make_qkv(w)
+    sigma = w.sigmas()
+    bins = plsh.sample_bins(n, sigma, s, seed=4)
+    q, k = to_dev(Q, "bf16"), to_dev(K, "bf16")
+    O1 = plsh.alibi_attn(q, k, to_dev(V, "bf16"), bins, True)
+    O2 = plsh.alibi_attn(q, k, to_dev(V * 4096.0, "bf16"), bins, True)
+    E1 = plsh.alibi_exact(q, k, to_dev(V, "bf16"), sigma, True)
+    E2 = plsh.alibi_exact(q, k, to_dev(V * 4096.0, "bf16"), sigma, True)
+    plsh.stream_status()
+    assert torch.equal(O2.float(), O1.float() * 4096.0)
+    assert torch.equal(E2.float(), E1.float() * 4096.0)
+    small = V * np.float32(2.0 ** -16)
+    O3 = plsh.alibi_attn(q, k, to_dev(small, "bf16"), bins, True)
+    plsh.stream_status()
+    off, st = oracle.sample_bins(n, sigma, s, seed=4)
+    rows = oracle.all_rows(1, 4, n)
+    ref = oracle.plsh_attn_rows(Q, K, small, off, st, s, True, rows)
+    got = gather_rows(O3, rows)
+    bound = 2e-3 * 2.0 ** -16 + 2.0 ** -24 + 1e-2 * np.abs(ref)
+    assert (np.abs(got - ref) <= bound).all(), np.abs(got - ref).max()
+    bins.free()
+
+
+@pytest.mark.parametrize("exact", [False, True], ids=["approx", "exact"])
+def test_v_beyond_f16_range_is_reported(exact):
+    """A value of V that rounds past f16's largest finite value (bf16 65536)
+    is reported as PLSH_ERR_RANGE by the next plsh_stream_status, which clears
+    the flag; 65280 (the largest bf16 value below it) is served."""
+    n, s = 300, 4
+    w = Workload("vrange", 1, 2, 1, n, 128, "bf16", True, s, (3.0, 30.0), qkv_seed=23)
+    Q, K, V = make_qkv(w)
+    bins = plsh.sample_bins(n, w.sigmas(), s, seed=1)
+    q, k = to_dev(Q, "bf16"), to_dev(K, "bf16")
+
+    def call(vv):
+        if exact:
+            return plsh.alibi_exact(q, k, to_dev(vv, "bf16"), w.sigmas(), True)
+        return plsh.alibi_attn(q, k, to_dev(vv, "bf16"), bins, True)
+
+    ok = V.copy()
+    ok[0, 0, 17, 5] = 65280.0
+    call(ok)
+    plsh.stream_status()
+    bad = V.copy()
+    bad[0, 0, 211, 77] = -65536.0
+    call(bad)
+    with pytest.raises(plsh.PlshError) as err:
+        plsh.stream_status()
+    assert err.value.status == plsh.PLSH_ERR_RANGE
+    plsh.stream_status()
+    bins.free()

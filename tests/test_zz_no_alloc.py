@@ -67,3 +67,41 @@ def test_noalloc_rejects_oversized_requests():
                                      bins.handle, 1, ctypes.byref(big), None)
     assert st == plsh.PLSH_ERR_UNSUPPORTED
     assert b"work items" in lib.plsh_last_error()
+
+
+def test_noalloc_timeout_is_reported_and_next_call_agrees(monkeypatch):
+    """A device-side wait of the allocation-free path that runs out is kept in
+    the fixed array's error word (the call itself cannot see it) and reported
+    by plsh_noalloc_status, which clears it; plsh_set_wait_limit_ns applies to
+    this path, and the next call agrees with plsh_alibi_attn."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    lib = plsh.load()
+    w = WORKLOADS["mistral"].with_(n=1024)
+    Q, K, V = make_qkv(w)
+    q, k, v = (torch.from_numpy(x).to(torch.bfloat16).cuda() for x in (Q, K, V))
+    bins = plsh.sample_bins(w.n, w.sigmas(), w.s, w.hash_seed)
+    ref = torch.empty_like(q)
+    _call(lib.plsh_alibi_attn, q, k, v, bins, w.causal, ref)
+    plsh.stream_status()
+    plsh.noalloc_status()                       # nothing pending
+    plsh.set_wait_limit_ns(20_000_000)         # 20 ms per wait
+    try:
+        monkeypatch.setenv("PLSH_FAULT", "stall")
+        out = torch.zeros_like(q)
+        _call(lib.plsh_alibi_attn_noalloc, q, k, v, bins, w.causal, out)
+        with pytest.raises(plsh.PlshError) as err:
+            plsh.noalloc_status()
+        assert err.value.status == plsh.PLSH_ERR_TIMEOUT
+        plsh.noalloc_status()                   # cleared by the report
+        plsh.stream_status()                    # the library's own flag is untouched
+    finally:
+        monkeypatch.delenv("PLSH_FAULT", raising=False)
+        plsh.set_wait_limit_ns(0)
+    again = torch.full_like(q, float("nan"))
+    _call(lib.plsh_alibi_attn_noalloc, q, k, v, bins, w.causal, again)
+    plsh.noalloc_status()
+    refd = ref.float().cpu().numpy()
+    got = again.float().cpu().numpy()
+    assert np.all(np.abs(got - refd) <= ATOL + RTOL * np.abs(refd))
+    bins.free()
