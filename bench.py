@@ -244,7 +244,23 @@ def run_ours(args, rank, world):
             plsh.alibi_attn(Q, K, V, bins, w.causal, out=O)
             e2.record(stream)
         torch.cuda.synchronize()
+        # clock soak: the same steps back to back for ~1.5 s, so that the
+        # clock record under load holds several samples (not part of value)
+        soak_steps = 0
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        t_end = time.perf_counter() + args.soak_seconds
+        while time.perf_counter() < t_end:
+            for _ in range(64):
+                bins.resample(sigma, seed)
+                plsh.alibi_attn(Q, K, V, bins, w.causal, out=O)
+            soak_steps += 64
+            torch.cuda.synchronize()
+        s1.record(stream)
+        torch.cuda.synchronize()
     plsh.stream_status()
+    soak_ms = s0.elapsed_time(s1) / max(1, soak_steps)
     step_ms = [a.elapsed_time(c) for a, c in ev_step]
     attn_ms = [b.elapsed_time(c) for a, b, c in ev]
     sample_ms = [a.elapsed_time(b) for a, b, c in ev]
@@ -348,13 +364,124 @@ def run_ours(args, rank, world):
                   "tflops": ex_flops / ex_avg_s / 1e12,
                   "frac": ex_flops / ex_avg_s / 1e12 / peak_tf},
         "approx_error_vs_exact": approx_err,
-        "clocks": clocks.summary(),
+        "clocks": dict(clocks.summary(), soak={"steps": soak_steps, "ms_per_step": soak_ms,
+                                               "l2": "not flushed (back to back)"}),
     }
     result["decode"] = measure_decode(w, bins, sigma, flush, stream)
     result["fixed_blocks"] = measure_fixed(w, sigma, Q, K, V, E, flush, stream)
+    if not args.no_configs:
+        del E
+        result["configs"] = measure_configs(flush, stream)
+        result["crossover"] = measure_crossover(flush, stream, result["configs"].get("scout"))
     if rank == 0 and not args.no_cpu:
         result["cpu_baseline"] = cpu_baseline(w, Qn, Kn, Vn, offsets, starts, args.cpu_seconds)
     return result
+
+
+# ------------------------------------------------ the other workloads
+CONFIG_NAMES = ["qwen_s10", "qwen_s20", "sweep_s1", "sweep_s5", "sweep_s10", "sweep_s20",
+                "sweep_s40", "scout"]
+
+
+def device_qkv(w, seed):
+    """N(0,1) Q, K, V of the workload's shape drawn on the device (seeded;
+    the timing lines do not need the oracle's host copies), with the peaky
+    rows of the Qwen-shaped workload."""
+    import torch
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    q = torch.randn(w.B, w.Hq, w.n, w.d, generator=g, device="cuda")
+    k = torch.randn(w.B, w.Hkv, w.n, w.d, generator=g, device="cuda")
+    v = torch.randn(w.B, w.Hkv, w.n, w.d, generator=g, device="cuda")
+    if w.peaky_frac > 0:
+        rows = torch.rand(w.B, w.n, generator=g, device="cuda") < w.peaky_frac
+        sc = torch.where(rows, w.peaky_scale, 1.0)[:, None, :, None]
+        q *= sc
+        k *= sc
+    return q.to(tdt), k.to(tdt), v.to(tdt)
+
+
+def time_calls(fn, flush, stream, iters):
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(iters):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    return statistics.median(ms)
+
+
+def approx_vs_exact(w, flush, stream, iters=5, exact_iters=3, seed=77):
+    """One workload: the fused kernel's time against its roofline (block
+    FLOPs at the tensor peak, bytes at the HBM peak, whichever is slower), the
+    exact kernel's time, and the approximation's error against exact ALiBi."""
+    import torch
+    import positional_lsh_approximation_gb300 as plsh
+    q, k, v = device_qkv(w, seed)
+    sigma = w.sigmas()
+    bins = plsh.sample_bins(w.n, sigma, w.s, w.hash_seed)
+    off, st = bins.to_host()
+    f_block, bytes_, mma, tiles = work_counts(w, off, st)
+    O = torch.empty_like(q)
+    t_a = time_calls(lambda: plsh.alibi_attn(q, k, v, bins, w.causal, out=O), flush, stream,
+                     iters)
+    E = torch.empty_like(q)
+    t_e = time_calls(lambda: plsh.alibi_exact(q, k, v, sigma, w.causal, out=E), flush, stream,
+                     exact_iters)
+    plsh.stream_status()
+    diff = O.float() - E.float()
+    err = float(diff.norm() / E.float().norm())
+    del diff, O, E, q, k, v
+    bins.free()
+    pk = peaks()
+    t_tc = f_block / (pk["bf16_tflops"] * 1e12)
+    t_hbm = bytes_ / (pk["hbm_gbs"] * 1e9)
+    ex_flops = 4.0 * w.d * w.B * w.Hq * (w.n * (w.n + 1) / 2 if w.causal else w.n * w.n)
+    sec = t_a / 1e3
+    return {"n": w.n, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "s": w.s,
+            "approx_ms": t_a, "tokens_per_s": w.B * w.n / sec,
+            "bound": "tensor" if t_tc >= t_hbm else "hbm",
+            "frac": max(t_tc, t_hbm) / sec,
+            "tensor_frac": f_block / sec / 1e12 / pk["bf16_tflops"],
+            "hbm_frac": bytes_ / sec / 1e9 / pk["hbm_gbs"],
+            "mma_frac_executed": mma / sec / 1e12 / pk["bf16_tflops"],
+            "flops_per_launch": f_block, "bytes_per_launch": bytes_,
+            "exact_ms": t_e, "exact_frac": ex_flops / (t_e / 1e3) / 1e12 / pk["bf16_tflops"],
+            "approx_over_exact_time": t_a / t_e,
+            "approx_error_vs_exact_rel_fro": err}
+
+
+def measure_configs(flush, stream):
+    """Every other workload's line, L2 flushed before each timed call."""
+    out = {}
+    for name in CONFIG_NAMES:
+        w = WORKLOADS[name]
+        out[name] = approx_vs_exact(w, flush, stream, exact_iters=2 if name == "scout" else 3)
+    return out
+
+
+def measure_crossover(flush, stream, scout=None):
+    """Approximation against exact ALiBi in wall-clock on the Scout-shaped
+    heads (40 query / 8 KV heads, d = 128, sigma = 256, s = 16) as n grows."""
+    w0 = WORKLOADS["scout"]
+    rows = []
+    for n in (16384, 32768, 65536, 131072):
+        if n == w0.n and scout is not None:
+            r = scout
+        else:
+            r = approx_vs_exact(w0.with_(n=n), flush, stream, exact_iters=3)
+        rows.append({"n": n, "approx_ms": r["approx_ms"], "exact_ms": r["exact_ms"],
+                     "speedup_over_exact": r["exact_ms"] / r["approx_ms"],
+                     "approx_error_vs_exact_rel_fro": r["approx_error_vs_exact_rel_fro"]})
+    return rows
 
 
 # ------------------------------------------------------- fixed blocks
@@ -554,8 +681,12 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="mistral", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other workloads' lines and the crossover sweep")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-positions", type=int, default=96)
+    ap.add_argument("--soak-seconds", type=float, default=1.5,
+                    help="back-to-back steps after the timed ones, for the clock record")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
