@@ -369,8 +369,11 @@ def run_ours(args, rank, world):
     }
     result["decode"] = measure_decode(w, bins, sigma, flush, stream)
     result["fixed_blocks"] = measure_fixed(w, sigma, Q, K, V, E, flush, stream)
+    result["shared_groups"] = measure_shared_groups(w, sigma, Q, K, V, E, flush, stream)
+    result["bias_error"] = measure_bias_error()
     if not args.no_configs:
         del E
+        result["split"] = measure_split(flush, stream)
         result["configs"] = measure_configs(flush, stream)
         result["crossover"] = measure_crossover(flush, stream, result["configs"].get("scout"))
     if rank == 0 and not args.no_cpu:
@@ -459,6 +462,30 @@ def approx_vs_exact(w, flush, stream, iters=5, exact_iters=3, seed=77):
             "approx_error_vs_exact_rel_fro": err}
 
 
+def measure_split(flush, stream):
+    """The key-range split of long work items on a case that needs it: one
+    pair of heads of a long sequence with wide bins (few items, envelopes of
+    up to ~100 key tiles), automatic split against none."""
+    import torch
+    import positional_lsh_approximation_gb300 as plsh
+    from positional_lsh_approximation_gb300.inputs import Workload
+    w = Workload("long_pair", 1, 2, 1, 16384, 128, "bf16", True, 10, (2000.0, 3000.0))
+    q, k, v = device_qkv(w, 5)
+    bins = plsh.sample_bins(w.n, w.sigmas(), w.s, w.hash_seed)
+    O = torch.empty_like(q)
+    out = {"workload": "B=1, 2 query heads / 1 KV head, n=16384, d=128, causal, s=10, "
+                       "sigma 2000 and 3000"}
+    for name, parts in (("unsplit", 1), ("automatic", 0)):
+        plsh.set_split_parts(parts)
+        out[name + "_ms"] = time_calls(lambda: plsh.alibi_attn(q, k, v, bins, True, out=O),
+                                       flush, stream, 10)
+    plsh.set_split_parts(0)
+    plsh.stream_status()
+    bins.free()
+    out["speedup"] = out["unsplit_ms"] / out["automatic_ms"]
+    return out
+
+
 def measure_configs(flush, stream):
     """Every other workload's line, L2 flushed before each timed call."""
     out = {}
@@ -482,6 +509,50 @@ def measure_crossover(flush, stream, scout=None):
                      "speedup_over_exact": r["exact_ms"] / r["approx_ms"],
                      "approx_error_vs_exact_rel_fro": r["approx_error_vs_exact_rel_fro"]})
     return rows
+
+
+# ------------------------------------------- hashes shared across a group
+def measure_shared_groups(w, sigma, Q, K, V, E, flush, stream, iters=10):
+    """Hashes shared by the query heads of a KV group (one draw per group at
+    the geometric mean of its heads' scales) against per-head hashes at equal
+    s: attention time on the same kernel and error against exact ALiBi."""
+    import torch
+    import positional_lsh_approximation_gb300 as plsh
+    G = w.Hq // w.Hkv
+    sg = [float(np.exp(np.mean(np.log(sigma[g * G:(g + 1) * G])))) for g in range(w.Hkv)]
+    src = plsh.sample_bins(w.n, sg, w.s, w.hash_seed)
+    sh = plsh.bins_share_groups(src, w.Hq)
+    O = torch.empty_like(Q)
+    t = time_calls(lambda: plsh.alibi_attn(Q, K, V, sh, w.causal, out=O), flush, stream, iters)
+    plsh.stream_status()
+    diff = O.float() - E.float()
+    err = float(diff.norm() / E.float().norm())
+    sh.free()
+    src.free()
+    return {"sigma_per_group": "geometric mean of the group's sigma_h", "s": w.s,
+            "attn_ms": t, "tokens_per_s": w.B * w.n / (t / 1e3), "rel_fro_vs_exact": err}
+
+
+# ---------------------------------------------------- bias error at scale
+def measure_bias_error(n=131072, sigma=256.0, ss=(4, 16, 64), iters=60):
+    """||L* - M~|| in max and spectral norm for one head at n = 131072 (the
+    Scout-shaped length, sigma = 256) as s grows: values, time per call (host
+    clock: the call blocks) and the fitted slope of the spectral error in
+    log s (the summary's O(1/sqrt(s)) convergence)."""
+    import positional_lsh_approximation_gb300 as plsh
+    rows = []
+    for s_ in ss:
+        b = plsh.sample_bins(n, [sigma], s_, 0)
+        plsh.bias_error(b, sigma, 0, lanczos_iters=8, seed=1)     # warm-up
+        t0 = time.perf_counter()
+        mx, sp = plsh.bias_error(b, sigma, 0, lanczos_iters=iters, seed=1)
+        dt = time.perf_counter() - t0
+        b.free()
+        rows.append({"s": s_, "max_abs": mx, "spectral": sp, "ms": dt * 1e3})
+    slope = float(np.polyfit(np.log([r["s"] for r in rows]),
+                             np.log([r["spectral"] for r in rows]), 1)[0])
+    return {"n": n, "sigma": sigma, "lanczos_iters": iters, "rows": rows,
+            "spectral_slope_vs_log_s": slope}
 
 
 # ------------------------------------------------------- fixed blocks

@@ -359,6 +359,24 @@ plsh_status plsh_attn_path(const plsh_tensor* Q, const plsh_bins* bins, int32_t 
  * this call on the current device (0 restores the default of 2 s). */
 plsh_status plsh_set_wait_limit_ns(uint64_t ns);
 
+/*
+ * plsh_set_split_parts -- how the tensor-core attention calls on the current
+ * device cut long work items over their key range (the varlen scheduling
+ * step: items are pairs of 128-row query tiles, each item's key envelope is
+ * found on the device from its rows' bins).
+ *   0   automatic (the default): an item whose expected key tiles exceed
+ *       half the call's per-SM share (at least 2) is cut into parts of at
+ *       most that size, so that no single item outlasts the others;
+ *   1   never cut;
+ *   2..16  cut every item into that many parts (a tuning and testing knob).
+ * Each part covers a consecutive range of its item's key tiles (a part past
+ * the envelope does nothing); parts write their unnormalised P V, running max
+ * and row sum to a library-owned workspace and a second kernel combines them
+ * into O.  Calls made afterwards use the setting; the workspace is allocated
+ * with the item table of a shape.
+ */
+plsh_status plsh_set_split_parts(int32_t parts);
+
 const char* plsh_status_string(plsh_status status);
 
 /* Message of the last error raised on the calling thread ("" if none). */

@@ -23,7 +23,8 @@ from . import build as _build_mod
 __all__ = ["build", "load", "sample_bins", "bins_from_host", "bins_fixed", "bins_share_groups", "Bins", "alibi_attn",
            "alibi_attn_noalloc", "alibi_attn_host",
            "alibi_exact", "alibi_decode", "alibi_attn_backward", "bias_error", "stream_status",
-           "noalloc_status", "attn_path", "set_wait_limit_ns", "PlshError", "library_path"]
+           "noalloc_status", "attn_path", "set_split_parts", "set_wait_limit_ns", "PlshError",
+           "library_path"]
 
 PLSH_OK, PLSH_ERR_INVALID, PLSH_ERR_CUDA, PLSH_ERR_NOMEM, PLSH_ERR_TIMEOUT, \
     PLSH_ERR_UNSUPPORTED, PLSH_ERR_RANGE = range(7)
@@ -92,6 +93,7 @@ def load():
             "plsh_noalloc_status": [P],
             "plsh_attn_path": [TP, P, I32, ctypes.POINTER(I32)],
             "plsh_set_wait_limit_ns": [U64],
+            "plsh_set_split_parts": [I32],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -354,6 +356,12 @@ def attn_path(Q, bins=None, causal: bool = True) -> str:
     _check(load().plsh_attn_path(ctypes.byref(t), bins.handle if bins is not None else None,
                                  int(bool(causal)), ctypes.byref(out)))
     return "tensor_cores" if out.value == PLSH_PATH_TENSOR_CORES else "cuda_cores"
+
+
+def set_split_parts(parts: int):
+    """plsh_set_split_parts: 0 automatic key-range split of long work items,
+    1 never, 2..16 every item in that many parts."""
+    _check(load().plsh_set_split_parts(int(parts)))
 
 
 def set_wait_limit_ns(ns: int):

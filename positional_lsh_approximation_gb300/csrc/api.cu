@@ -2,6 +2,7 @@
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
+#include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
 
@@ -232,16 +233,42 @@ plsh_status check_qkvo(const plsh_tensor* Q, const plsh_tensor* K, const plsh_te
   return PLSH_OK;
 }
 
+// Expected key tiles of an item: the exact kernel takes every key tile up to
+// the diagonal (every key tile without the causal mask); the approximation
+// the diagonal tile plus its rows' look-back, about 1.5 sigma (1 + 0.7 ln s)
+// keys (the mean age of the Gamma(2, sigma) bin that holds a row is 1.5 sigma;
+// the largest of s such ages grows like ln s; the factor 0.7 matches the
+// envelopes measured at s = 10).
+double expected_tiles(bool exact, bool causal, int QT, int qt, double sigma, int s) {
+  if (exact) return causal ? qt + 1 : QT;
+  const double back = 1.5 * sigma * (1.0 + 0.7 * log((double)std::max(s, 1)));
+  const double t = 1.0 + ceil(back / 128.0);
+  return causal ? std::min((double)(qt + 1), t) : std::min((double)QT, 2.0 * t - 1.0);
+}
+
+struct ItemList {
+  std::vector<int4> items, ext, merge;
+};
+
 // Items of the tensor-core kernel: two 128-row query tiles sharing one KV
 // head.  Heads of a KV group pair up (sorted by sigma so that paired heads
 // have similar key envelopes); an odd group's last head pairs its own row
 // tiles.  Ordered by expected cost, largest first, so that the dynamic queue
 // balances like longest-processing-time scheduling.
-std::vector<int4> build_items(int B, int Hq, int Hkv, int qt0, int qt1, bool exact,
-                              const std::vector<double>& sigma) {
+//
+// Key-range split: with split_parts = 0 an item whose expected key tiles
+// exceed half the per-SM share of the whole call (at least 2) is cut into
+// parts of at most that size, so that the longest-first queue can even the
+// SMs out (pieces of a whole share would still leave one SM with a piece plus
+// an item); with
+// split_parts >= 2 every item is cut into that many parts; 1 never splits.
+// The parts of an item follow it in the order and cover consecutive key
+// ranges of its envelope.
+ItemList build_items(int B, int Hq, int Hkv, int QT, int qt0, int qt1, bool exact, bool causal,
+                     int s, int num_sms, int split_parts, const std::vector<double>& sigma) {
   const int G = Hq / Hkv;
   std::vector<int4> items;
-  std::vector<double> cost;
+  std::vector<double> cost, tiles;
   items.reserve((size_t)B * Hq * (qt1 - qt0) / 2 + B * Hkv);
   for (int b = 0; b < B; ++b) {
     for (int kvh = 0; kvh < Hkv; ++kvh) {
@@ -252,48 +279,105 @@ std::vector<int4> build_items(int B, int Hq, int Hkv, int qt0, int qt1, bool exa
                          [&](int x, int y) { return sigma[x] > sigma[y]; });
       for (int pr = 0; pr + 1 < G; pr += 2) {
         const int hA = heads[pr], hB = heads[pr + 1];
+        const double sg = exact ? 0.0 : std::max(sigma[hA], sigma[hB]);
         for (int qt = qt0; qt < qt1; ++qt) {
           items.push_back(make_int4(b, hA | (hB << 16), qt, qt));
-          cost.push_back(exact ? (double)qt : std::max(sigma[hA], sigma[hB]) * 1e6 + qt);
+          cost.push_back(exact ? (double)qt : sg * 1e6 + qt);
+          tiles.push_back(expected_tiles(exact, causal, QT, qt, sg, s));
         }
       }
       if (G % 2) {
         const int hL = heads[G - 1];
+        const double sg = exact ? 0.0 : sigma[hL];
         for (int qt = qt0; qt < qt1; qt += 2) {
           const int qtB = qt + 1 < qt1 ? qt + 1 : -1;
           items.push_back(make_int4(b, hL | (hL << 16), qt, qtB));
-          cost.push_back(exact ? (double)std::max(qt, qtB) : sigma[hL] * 1e6 + qt);
+          cost.push_back(exact ? (double)std::max(qt, qtB) : sg * 1e6 + qt);
+          tiles.push_back(expected_tiles(exact, causal, QT, std::max(qt, qtB), sg, s) + 1.0);
         }
       }
     }
+  }
+  // parts per item
+  std::vector<int> parts(items.size(), 1);
+  if (split_parts >= 2) {
+    std::fill(parts.begin(), parts.end(), std::min(split_parts, plsh::kMaxSplitParts));
+  } else if (split_parts == 0 && num_sms > 0) {
+    double total = 0.0;
+    for (double t : tiles) total += t;
+    const double cap = std::max(2.0, ceil(0.5 * total / num_sms));
+    for (size_t k = 0; k < items.size(); ++k)
+      if (tiles[k] > cap)
+        parts[k] = (int)std::min((double)plsh::kMaxSplitParts, ceil(tiles[k] / cap));
   }
   std::vector<size_t> order(items.size());
   std::iota(order.begin(), order.end(), 0);
   std::stable_sort(order.begin(), order.end(),
                    [&](size_t x, size_t y) { return cost[x] > cost[y]; });
-  std::vector<int4> sorted(items.size());
-  for (size_t k = 0; k < order.size(); ++k) sorted[k] = items[order[k]];
-  return sorted;
+  ItemList out;
+  bool any_split = false;
+  for (int pc : parts) any_split = any_split || pc > 1;
+  int slot = 0;
+  for (size_t k = 0; k < order.size(); ++k) {
+    const int4 it = items[order[k]];
+    const int pc = parts[order[k]];
+    if (pc > 1) {
+      out.merge.push_back(it);
+      out.merge.push_back(make_int4(slot, pc, 0, 0));
+    }
+    for (int p = 0; p < pc; ++p) {
+      out.items.push_back(it);
+      if (any_split) out.ext.push_back(make_int4(p, pc, pc > 1 ? slot + p : -1, 0));
+    }
+    if (pc > 1) slot += pc;
+  }
+  return out;
 }
 
 // Device copy of the item table for this shape and head order (built and
-// uploaded on first use, then reused).
-plsh_status item_table(plsh::DeviceCtx* ctx, int B, int Hq, int Hkv, int qt0, int qt1,
-                       bool exact, const std::vector<double>& sigma, cudaStream_t st,
-                       const int4** out, int* count) {
-  // the table depends on the shape, the range of query tiles and, for the
-  // approximate kernel, on the order of sigma inside each KV group and across
-  // heads
-  std::string key = std::to_string(exact) + ":" + std::to_string(B) + ":" + std::to_string(Hq) +
-                    ":" + std::to_string(Hkv) + ":" + std::to_string(qt0) + "-" +
-                    std::to_string(qt1);
+// uploaded on first use, then reused), with the split parts' extra entries,
+// merge list and workspace when some item is split.
+struct TableRef {
+  const int4* items = nullptr;
+  int count = 0;
+  const int4* ext = nullptr;
+  const int4* merge = nullptr;
+  int merges = 0;
+  float* ws = nullptr;
+};
+
+void free_table(plsh::ItemTable& t) {
+  cudaFree(t.dev);
+  cudaFree(t.dev_ext);
+  cudaFree(t.dev_merge);
+  cudaFree(t.ws);
+}
+
+plsh_status item_table(plsh::DeviceCtx* ctx, int B, int Hq, int Hkv, int QT, int qt0, int qt1,
+                       bool exact, bool causal, int s, const std::vector<double>& sigma,
+                       cudaStream_t st, TableRef* out) {
+  // the table depends on the shape, the range of query tiles, the split
+  // setting and, for the approximate kernel, on the order of sigma inside
+  // each KV group and across heads (and on s and sigma through the split)
+  std::string key = std::to_string(exact) + ":" + std::to_string(causal) + ":" +
+                    std::to_string(B) + ":" + std::to_string(Hq) + ":" + std::to_string(Hkv) +
+                    ":" + std::to_string(QT) + ":" + std::to_string(qt0) + "-" +
+                    std::to_string(qt1) + ":split" + std::to_string(ctx->split_parts);
   if (!exact) {
     std::vector<int> rank(Hq);
     std::iota(rank.begin(), rank.end(), 0);
     std::stable_sort(rank.begin(), rank.end(),
                      [&](int x, int y) { return sigma[x] > sigma[y]; });
-    key.push_back(':');
+    key += ":s" + std::to_string(s) + ":";
     for (int h : rank) key += std::to_string(h) + ",";
+    if (ctx->split_parts == 0) {
+      // the automatic split follows the scales themselves
+      char buf[32];
+      for (double v : sigma) {
+        snprintf(buf, sizeof buf, "%.6g,", v);
+        key += buf;
+      }
+    }
   }
   std::lock_guard<std::mutex> lk(g_ctx_mu);
   auto it = ctx->tables.find(key);
@@ -303,24 +387,50 @@ plsh_status item_table(plsh::DeviceCtx* ctx, int B, int Hq, int Hkv, int qt0, in
       for (auto jt = ctx->tables.begin(); jt != ctx->tables.end(); ++jt)
         if (jt->second.last_use < victim->second.last_use) victim = jt;
       cudaDeviceSynchronize();
-      cudaFree(victim->second.dev);
+      free_table(victim->second);
       ctx->tables.erase(victim);
     }
     plsh::ItemTable t;
-    t.host = build_items(B, Hq, Hkv, qt0, qt1, exact, sigma);
-    plsh_status s = dev_alloc((void**)&t.dev, sizeof(int4) * t.host.size(), "item table");
-    if (s != PLSH_OK) return s;
+    ItemList lst = build_items(B, Hq, Hkv, QT, qt0, qt1, exact, causal, s, ctx->num_sms,
+                               ctx->split_parts, sigma);
+    t.host = std::move(lst.items);
+    t.ext = std::move(lst.ext);
+    t.merge = std::move(lst.merge);
+    int slots = 0;
+    for (size_t k = 1; k < t.merge.size(); k += 2) slots += t.merge[k].y;
+    plsh_status s1 = dev_alloc((void**)&t.dev, sizeof(int4) * t.host.size(), "item table");
+    if (s1 == PLSH_OK && !t.ext.empty())
+      s1 = dev_alloc((void**)&t.dev_ext, sizeof(int4) * t.ext.size(), "item table");
+    if (s1 == PLSH_OK && !t.merge.empty())
+      s1 = dev_alloc((void**)&t.dev_merge, sizeof(int4) * t.merge.size(), "item table");
+    if (s1 == PLSH_OK && slots > 0)
+      s1 = dev_alloc((void**)&t.ws, sizeof(float) * plsh::kSplitSlotFloats * slots,
+                     "split workspace");
+    if (s1 != PLSH_OK) {
+      free_table(t);
+      return s1;
+    }
     cudaError_t e = cudaMemcpyAsync(t.dev, t.host.data(), sizeof(int4) * t.host.size(),
                                     cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess && !t.ext.empty())
+      e = cudaMemcpyAsync(t.dev_ext, t.ext.data(), sizeof(int4) * t.ext.size(),
+                          cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess && !t.merge.empty())
+      e = cudaMemcpyAsync(t.dev_merge, t.merge.data(), sizeof(int4) * t.merge.size(),
+                          cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess) {
-      cudaFree(t.dev);
+      free_table(t);
       return cuda_fail(e, "item table upload");
     }
     it = ctx->tables.emplace(key, std::move(t)).first;
   }
   it->second.last_use = ++ctx->table_clock;
-  *out = it->second.dev;
-  *count = (int)it->second.host.size();
+  out->items = it->second.dev;
+  out->count = (int)it->second.host.size();
+  out->ext = it->second.dev_ext;
+  out->merge = it->second.dev_merge;
+  out->merges = (int)it->second.merge.size() / 2;
+  out->ws = it->second.ws;
   return PLSH_OK;
 }
 
@@ -388,16 +498,25 @@ plsh_status run_attention(const plsh_tensor* Q, const plsh_tensor* K, const plsh
   if (path == Path::Tc && !tc_ok)
     return fail(PLSH_ERR_UNSUPPORTED, "tensor-core path needs bf16, d = 128 and s within "
                                       "its shared-memory budget");
+  TableRef tab;
   if (path == Path::Tc) {
     const int QT = (int)((Q->n + 127) / 128);
-    plsh_status s1 = item_table(ctx, a.B, a.Hq, a.Hkv, qt0, qt1 < 0 ? QT : qt1, a.exact != 0,
-                                bins ? bins->sigma_host : std::vector<double>(), st,
-                                &a.items, &a.num_items);
+    plsh_status s1 = item_table(ctx, a.B, a.Hq, a.Hkv, QT, qt0, qt1 < 0 ? QT : qt1, a.exact != 0,
+                                a.causal != 0, a.s,
+                                bins ? bins->sigma_host : std::vector<double>(), st, &tab);
     if (s1 != PLSH_OK) return s1;
+    a.items = tab.items;
+    a.num_items = tab.count;
+    a.item_ext = tab.ext;
+    a.split_ws = tab.ws;
   }
   cudaError_t e = path == Path::Tc ? plsh::launch_attn_tc(a, slopes, ctx->num_sms, st)
                                    : plsh::launch_attn_simt(a, slopes, Q->dtype, st);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+  if (path == Path::Tc && tab.merges > 0) {
+    e = plsh::launch_split_merge(tab.merge, tab.merges, tab.ws, a.O, a.Hq, a.n, st);
+    if (e != cudaSuccess) return cuda_fail(e, "split merge launch");
+  }
   return PLSH_OK;
 }
 
@@ -885,7 +1004,8 @@ plsh_status plsh_alibi_decode(const plsh_tensor* q, const plsh_tensor* K, const 
   plsh::DeviceCtx* ctx = nullptr;
   if ((st = current_ctx(&ctx)) != PLSH_OK) return st;
   const size_t bytes =
-      sizeof(float) * plsh::decode_work_floats((int)q->B, (int)q->H, (int)q->d, ctx->num_sms);
+      sizeof(float) * plsh::decode_work_floats((int)q->B, (int)q->H, (int)K->H, (int)q->d,
+                                               ctx->num_sms);
   float* work = nullptr;
   {
     std::lock_guard<std::mutex> lk(g_ctx_mu);
@@ -918,6 +1038,8 @@ plsh_status plsh_alibi_decode(const plsh_tensor* q, const plsh_tensor* K, const 
   a.dtype = q->dtype;
   a.num_sms = ctx->num_sms;
   a.work = work;
+  a.err = ctx->d_err;
+  a.wait_ns = ctx->wait_ns;
   PLSH_TRY_CUDA(plsh::launch_decode(a, (cudaStream_t)stream), "decode launch");
   return PLSH_OK;
 }
@@ -947,6 +1069,16 @@ plsh_status plsh_stream_status(void* stream) {
     PLSH_TRY_CUDA(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
   }
   return device_flag_status(flag);
+}
+
+plsh_status plsh_set_split_parts(int32_t parts) {
+  if (parts < 0 || parts > plsh::kMaxSplitParts)
+    return fail(PLSH_ERR_INVALID, "parts must be in [0, " + std::to_string(plsh::kMaxSplitParts) + "]");
+  plsh::DeviceCtx* ctx = nullptr;
+  plsh_status st = current_ctx(&ctx);
+  if (st != PLSH_OK) return st;
+  ctx->split_parts = parts;
+  return PLSH_OK;
 }
 
 plsh_status plsh_set_wait_limit_ns(uint64_t ns) {

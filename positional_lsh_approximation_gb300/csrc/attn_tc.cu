@@ -54,6 +54,7 @@
 // on expiry the CTA raises the library error flag, drains its in-flight copies
 // and MMAs, frees TMEM and exits.
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <limits.h>
@@ -110,6 +111,7 @@ constexpr int kErrRange = 2;
 
 struct Item {
   int valid, b, hA, hB, qtA, qtB, kt_lo, kt_hi;
+  int ws;                    // workspace slot of a split part, -1 for a whole item
 };
 
 struct Ctl {
@@ -141,6 +143,7 @@ __device__ __forceinline__ Item read_item(const Ctl* ctl, int slot) {
   Item it;
   it.valid = v[0]; it.b = v[1]; it.hA = v[2]; it.hB = v[3];
   it.qtA = v[4]; it.qtB = v[5]; it.kt_lo = v[6]; it.kt_hi = v[7];
+  it.ws = v[8];
   return it;
 }
 
@@ -321,19 +324,22 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
     for (int seq = 0; !a.stall; ++seq) {   // stall: fault injection
       const int slot = seq % kRing;
       const uint32_t use = (uint32_t)(seq / kRing);
-      int idx = 0;
-      if (lane == 0) {
-        ok = mbar_wait(bar(B_IEMPTY + slot), (use & 1u) ^ 1u, abort, lim);
-        if (ok) idx = atomicAdd(a.queue, 1);
-      }
+      if (lane == 0) ok = mbar_wait(bar(B_IEMPTY + slot), (use & 1u) ^ 1u, abort, lim);
       ok = __shfl_sync(FULL, (int)ok, 0) != 0;
-      idx = __shfl_sync(FULL, idx, 0);
       if (!ok) break;
+      // pop until an item with work (a split item's part past its key
+      // envelope only marks its rows empty) or the end of the queue
+      bool published = false, drained = false;
+      while (!published) {
+      int idx = 0;
+      if (lane == 0) idx = atomicAdd(a.queue, 1);
+      idx = __shfl_sync(FULL, idx, 0);
       if (idx >= a.num_items) {
         if (lane == 0) {
           ctl->ring[slot].valid = 0;
           mbar_arrive(bar(B_IFULL + slot));
         }
+        drained = true;
         break;
       }
       const int4 e4 = __ldg(a.items + idx);
@@ -398,13 +404,39 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       }
       kt_lo = min(kt_lo, qmax);
       kt_hi = max(kt_hi, kt_lo + 1);
+      int ws = -1;
+      if (a.item_ext != nullptr) {
+        // part x.x of x.y over the key tiles of the envelope
+        const int4 x = __ldg(a.item_ext + idx);
+        if (x.y > 1) {
+          const int len = kt_hi - kt_lo;
+          const int lo_p = kt_lo + (len * x.x) / x.y;
+          const int hi_p = kt_lo + (len * (x.x + 1)) / x.y;
+          ws = x.z;
+          if (hi_p <= lo_p) {
+            // no key tile: every row of the part has no weight
+            float* wm = a.split_ws + (size_t)ws * kSplitSlotFloats + 2 * BM * kSplitRowFloats;
+            for (int k = lane; k < 2 * BM; k += 32) {
+              wm[k] = -INFINITY;        // max
+              wm[2 * BM + k] = 0.f;     // row sum
+            }
+            __syncwarp();
+            continue;
+          }
+          kt_lo = lo_p;
+          kt_hi = hi_p;
+        }
+      }
       if (lane == 0) {
         volatile int* it = reinterpret_cast<volatile int*>(&ctl->ring[slot]);
         it[0] = 1; it[1] = b; it[2] = hA; it[3] = hB; it[4] = qtA; it[5] = qtB;
-        it[6] = kt_lo; it[7] = kt_hi;
+        it[6] = kt_lo; it[7] = kt_hi; it[8] = ws;
         mbar_arrive(bar(B_IFULL + slot));
       }
       __syncwarp();
+      published = true;
+      }
+      if (drained) break;
     }
     if (!ok && lane == 0) {
       *abort = 1;
@@ -580,7 +612,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       // before, so that Q loads and epilogues overlap tensor work
       int seq = 0;
       ok = mbar_wait(bar(B_IFULL + 0), 0u, abort, lim);
-      Item cur = ok ? read_item(ctl, 0) : Item{0, 0, 0, 0, 0, 0, 0, 0};
+      Item cur = ok ? read_item(ctl, 0) : Item{0, 0, 0, 0, 0, 0, 0, 0, -1};
       int T = cur.kt_hi - cur.kt_lo, jj = 0;
       bool have_prev = false;
       int prev_lv = 0, prev_slot = 0;
@@ -685,7 +717,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
     // starts in registers the set-up is short and the output goes first
     constexpr bool kDefer = SREG == 0;
     bool pend = false;
-    float pend_l = 0.f;
+    float pend_l = 0.f, pend_m = 0.f;
     const uint32_t obuf = sbase + off_out + (uint32_t)warp * 4096u;
     // epilogue of item pseq: O_i = acc_i / l_i, then its item slot is released
     auto finish = [&](int pseq) -> bool {
@@ -699,6 +731,29 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       const int h = tile ? pit.hB : pit.hA;
       const int i = max(qt, 0) * BM + r;
       const int64_t row0 = ((int64_t)pit.b * Hq + h) * n;
+      if (pit.ws >= 0) {
+        // a part of a split item: its unnormalised P V, max and row sum go
+        // to its workspace slot, to be combined with the other parts
+        float* w = a.split_ws + (size_t)pit.ws * kSplitSlotFloats;
+        float4* acc = reinterpret_cast<float4*>(w + ((size_t)tile * BM + r) * kSplitRowFloats);
+#pragma unroll 1
+        for (int q2 = 0; q2 < 4; ++q2) {
+          uint32_t o[32];
+          tmem_ld32(o_col + q2 * 32, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            acc[q2 * 8 + v] = make_float4(__uint_as_float(o[4 * v]), __uint_as_float(o[4 * v + 1]),
+                                          __uint_as_float(o[4 * v + 2]),
+                                          __uint_as_float(o[4 * v + 3]));
+        }
+        w[2 * BM * kSplitRowFloats + tile * BM + r] = pend_m;
+        w[2 * BM * kSplitRowFloats + 2 * BM + tile * BM + r] = pend_l;
+        tc_fence_before();
+        mbar_arrive(bar(B_IEMPTY + pslot));
+        pend = false;
+        return true;
+      }
       const float inv_l = pend_l > 0.f ? 1.f / pend_l : 0.f;
 #pragma unroll 1
       for (int q2 = 0; q2 < 2; ++q2) {
@@ -1210,6 +1265,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       // so that the item's last P V runs meanwhile
       pend = true;
       pend_l = l;
+      pend_m = (row_ok && l > 0.f) ? m_ref : -INFINITY;
       if (!kDefer) {
         ok = finish(seq);
         if (!ok) break;
@@ -1236,6 +1292,51 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       __threadfence();
     }
   }
+}
+
+// ----------------------------------------------------------- split merge
+// The parts of a split item cover disjoint key ranges of its rows' envelopes,
+// each with its own running max m_p (log2 units) and row sum l_p:
+//   O_i = sum_p 2^(m_p - m) acc_p / sum_p 2^(m_p - m) l_p,  m = max_p m_p,
+// over the parts that saw a key of row i (l_p > 0).  A warp per row, a float4
+// of the head dimension per lane.  Grid: (split items, 2 tiles, 16 row groups).
+__global__ void __launch_bounds__(256)
+split_merge_kernel(const int4* __restrict__ merge, const float* __restrict__ ws,
+                   __nv_bfloat16* __restrict__ O, int Hq, int n) {
+  const int item = blockIdx.x, tile = blockIdx.y;
+  const int r = blockIdx.z * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  const int4 e = merge[2 * item], x = merge[2 * item + 1];
+  const int qt = tile ? e.w : e.z;
+  const int h = tile ? (e.y >> 16) & 0xffff : e.y & 0xffff;
+  const int i = qt * BM + r;
+  if (qt < 0 || i >= n) return;
+  const int slot0 = x.x, parts = x.y;
+  float m = -INFINITY;
+  for (int p = 0; p < parts; ++p) {
+    const float* w = ws + (size_t)(slot0 + p) * kSplitSlotFloats + 2 * BM * kSplitRowFloats;
+    if (w[2 * BM + tile * BM + r] > 0.f) m = fmaxf(m, w[tile * BM + r]);
+  }
+  float l = 0.f;
+  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int p = 0; p < parts; ++p) {
+    const float* w = ws + (size_t)(slot0 + p) * kSplitSlotFloats;
+    const float* wm = w + 2 * BM * kSplitRowFloats;
+    const float lp = wm[2 * BM + tile * BM + r];
+    if (!(lp > 0.f)) continue;
+    const float f = exp2f(wm[tile * BM + r] - m);
+    l = fmaf(f, lp, l);
+    const float4 a4 =
+        reinterpret_cast<const float4*>(w + ((size_t)tile * BM + r) * kSplitRowFloats)[lane];
+    o.x = fmaf(f, a4.x, o.x);
+    o.y = fmaf(f, a4.y, o.y);
+    o.z = fmaf(f, a4.z, o.z);
+    o.w = fmaf(f, a4.w, o.w);
+  }
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  __nv_bfloat162* out =
+      reinterpret_cast<__nv_bfloat162*>(O + (((int64_t)e.x * Hq + h) * n + i) * HD) + 2 * lane;
+  out[0] = __floats2bfloat162_rn(o.x * inv, o.y * inv);
+  out[1] = __floats2bfloat162_rn(o.z * inv, o.w * inv);
 }
 
 // ------------------------------------------------------------------- host
@@ -1331,6 +1432,14 @@ bool out_staged(int s, int causal, int exact) {
 
 size_t attn_tc_smem_bytes(int s, int causal, int exact) {
   return smem_for(kSlots, out_staged(s, causal, exact), s, causal, exact);
+}
+
+cudaError_t launch_split_merge(const int4* merge, int count, const float* ws, void* O, int Hq,
+                               int n, cudaStream_t st) {
+  if (count <= 0) return cudaSuccess;
+  split_merge_kernel<<<dim3((unsigned)count, 2, BM / 8), 256, 0, st>>>(
+      merge, ws, static_cast<__nv_bfloat16*>(O), Hq, n);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_attn_tc(const AttnArgs& a, const float* slopes_host,

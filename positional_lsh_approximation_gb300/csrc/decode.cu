@@ -11,77 +11,59 @@
 // over j in [min_t lo_t(pos), pos]: a short attention over the row's key
 // envelope with integer weights, bound by the bytes of K and V it reads.
 //
-// Work is split over the envelope (flash-decoding style): each (batch
-// element, head) gets S splits (S chosen on the host so that the GPU holds
-// enough warps), a warp per split.  The warp finds the row's envelope from
-// its s bin records, takes its share of it in blocks of 64 keys with an
-// online softmax (scores a key per lane, P V with a row slice of 16 bytes per
-// lane, no block-wide barrier anywhere) and writes its max m, row sum l and
-// unnormalised P V; a second kernel merges the S splits of each (batch
-// element, head) and writes O = P V / l.
+// A CTA serves the query heads of one KV group (up to eight, a warp each) of
+// one batch element, over a share of the union of their envelopes (the work
+// is split over the envelope, flash-decoding style, so that the GPU holds
+// about three CTAs per SM).  The group's key and value rows of a block (16 KB
+// of each) arrive in shared memory by bulk asynchronous copies, double
+// buffered, completing on an mbarrier with a bounded wait (a copy per key row
+// into rows padded by 16 bytes, one copy for the value rows); every head of
+// the group then reads them from shared memory: scores with a key per lane
+// (the padding puts the same 16-byte chunk of consecutive rows in different
+// banks, and every lane reads the same chunk of the query), an online softmax
+// per head, P V with a slice of every row per lane.  Each (batch element, head, share) writes its max m, row
+// sum l and unnormalised P V; a second kernel merges the shares into
+// O = P V / l.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "bins_dev.cuh"
 #include "plsh_internal.h"
+#include "tc_ptx.cuh"
 
 namespace plsh {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
+using namespace ptx;
 
-template <typename T> struct Vec;
-template <> struct Vec<__nv_bfloat16> {
-  // raw 16 bytes of a row, converted element by element where they are used
-  using Raw = uint4;
-  __device__ static Raw raw(const __nv_bfloat16* p) { return *reinterpret_cast<const uint4*>(p); }
-  __device__ static float elem(const Raw& r, int e) {
-    const uint32_t w = e < 2 ? r.x : (e < 4 ? r.y : (e < 6 ? r.z : r.w));
-    return __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
-  }
+constexpr int kStageBytes = 16384;        // bytes of K (and of V) per block
+constexpr unsigned FULL = 0xffffffffu;
+
+// 1-D bulk copy global -> shared memory, completion counted in bytes on an
+// mbarrier of this CTA (both addresses 16-byte aligned, size a multiple of 16)
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+template <typename T> struct Elem;
+template <> struct Elem<__nv_bfloat16> {
   __device__ static float one(const __nv_bfloat16* p) { return __bfloat162float(*p); }
   __device__ static void store(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 };
-template <> struct Vec<float> {
-  struct Raw {
-    float4 a, b;
-  };
-  __device__ static Raw raw(const float* p) {
-    return Raw{*reinterpret_cast<const float4*>(p), *reinterpret_cast<const float4*>(p + 4)};
-  }
-  __device__ static float elem(const Raw& r, int e) {
-    const float4& h = e < 4 ? r.a : r.b;
-    const int k = e & 3;
-    return k == 0 ? h.x : (k == 1 ? h.y : (k == 2 ? h.z : h.w));
-  }
+template <> struct Elem<float> {
   __device__ static float one(const float* p) { return *p; }
   __device__ static void store(float* p, float v) { *p = v; }
 };
 
-// q . k over one row of D elements, eight per load, half a bf16 row (a
-// quarter of an fp32 row) in flight at a time
-template <typename T, int D>
-__device__ __forceinline__ float row_dot(const float* __restrict__ qs, const T* __restrict__ k) {
-  constexpr int L = sizeof(T) == 2 ? D / 16 : D / 32;  // loads in flight (64 bytes each lane)
-  float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-  for (int e0 = 0; e0 < D; e0 += 8 * L) {
-    typename Vec<T>::Raw r[L];
-#pragma unroll
-    for (int u = 0; u < L; ++u) r[u] = Vec<T>::raw(k + e0 + 8 * u);
-#pragma unroll
-    for (int u = 0; u < L; ++u) {
-#pragma unroll
-      for (int e = 0; e < 8; e += 2) {
-        a0 = fmaf(qs[e0 + 8 * u + e], Vec<T>::elem(r[u], e), a0);
-        a1 = fmaf(qs[e0 + 8 * u + e + 1], Vec<T>::elem(r[u], e + 1), a1);
-      }
-    }
-  }
-  return a0 + a1;
-}
+// the 2 (f32) or 4 (bf16) consecutive values of a 32-bit word pair / quad
+__device__ __forceinline__ float lo16(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float hi16(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
 struct DecodeParams {
   const void* q;        // [B, Hq, 1, D]
@@ -91,50 +73,55 @@ struct DecodeParams {
   int B, Hq, Hkv, n, s;
   int64_t W;
   int pos;
-  int splits;           // S
-  float* part_m;        // [B * Hq * S]
+  int heads;            // query heads per CTA (<= 8)
+  int hchunks;          // CTAs per KV group and share
+  int splits;           // shares of the envelope
+  float* part_m;        // [B * Hq * splits]
   float* part_l;
-  float* part_o;        // [B * Hq * S][D]
+  float* part_o;        // [B * Hq * splits][D]
+  int* err;
+  uint64_t wait_ns;
 };
 
-constexpr int kBlockKeys = 64;            // keys a warp scores at a time
-
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-__device__ __forceinline__ int warp_min_int(int v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
+template <typename T, int D>
+struct Cfg {
+  static constexpr int kRowBytes = D * (int)sizeof(T);
+  static constexpr int kKeys = kStageBytes / kRowBytes;        // keys per block
+  static constexpr int kChunks = kRowBytes / 16;               // 16-byte chunks of a row
+  static constexpr int kE = 16 / (int)sizeof(T);               // values per chunk
+  static constexpr int kPV = D / 32;                           // values of a row per lane
+  static constexpr int kKStride = kRowBytes + 16;              // padded key row
+  static constexpr uint32_t kKStage = (uint32_t)(kKeys * kKStride);
+  static constexpr uint32_t kSmem = 2u * kKStage + 2u * kStageBytes;  // K, V x two stages
+};
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kThreads, 3)
-decode_partial_kernel(DecodeParams p) {
-  constexpr int S8 = D / 8;               // lanes per row in P V (16 bytes of bf16 each)
-  constexpr int R = 32 / S8;              // rows per warp-wide load
-  __shared__ float qs_all[kWarps][D];
-  __shared__ float ps_all[kWarps][kBlockKeys];
-  __shared__ int los_all[kWarps][kMaxS];
+__global__ void __launch_bounds__(256)
+decode_group_kernel(DecodeParams p) {
+  using C = Cfg<T, D>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ float qs_all[8][D];
+  __shared__ float ps_all[8][C::kKeys];
+  __shared__ int los_all[8][kMaxS];
+  __shared__ int lo_warp[8];
+  __shared__ __align__(8) uint64_t full[2];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int item = blockIdx.x * kWarps + warp;
-  if (item >= p.B * p.Hq * p.splits) return;   // whole warps only
+  const int G = p.Hq / p.Hkv;
+  int cta = blockIdx.x;
+  const int split = cta % p.splits;
+  cta /= p.splits;
+  const int hc = cta % p.hchunks;
+  cta /= p.hchunks;
+  const int g = cta % p.Hkv, b = cta / p.Hkv;
+  const int hg = hc * p.heads + warp;                // head within the group
+  const bool valid = hg < G;
+  const int h = g * G + (valid ? hg : 0);
   float* qs = qs_all[warp];
   float* ps = ps_all[warp];
   int* los = los_all[warp];
-  const int bh = item / p.splits, split = item % p.splits;
-  const int b = bh / p.Hq, h = bh % p.Hq;
-  const int kvh = h / (p.Hq / p.Hkv);
+  const volatile int* no_abort = nullptr;
 
-  // the row's bin start under every hash of head h (s <= 64), its minimum,
-  // and the query in log2 units
+  // this head's bin start under every hash (s <= 64), the query in log2 units
   int lo_a = p.pos, lo_b = p.pos;
   const int64_t rbase = (int64_t)h * p.s * p.W + (p.pos >> 5);
   if (lane < p.s) lo_a = bin_lo(load_record(p.rec, rbase + (int64_t)lane * p.W), p.pos);
@@ -142,108 +129,209 @@ decode_partial_kernel(DecodeParams p) {
   los[lane] = lo_a;
   los[lane + 32] = lo_b;
   const float scale = 1.4426950408889634f * rsqrtf((float)D);   // log2(e) / sqrt(d)
-  const T* q = static_cast<const T*>(p.q) + (int64_t)bh * D;
-  for (int e = lane; e < D; e += 32) qs[e] = Vec<T>::one(q + e) * scale;
-  const int lo_min = warp_min_int(min(lo_a, lo_b));
-  __syncwarp();
+  const T* q = static_cast<const T*>(p.q) + ((int64_t)b * p.Hq + h) * D;
+  for (int e = lane; e < D; e += 32) qs[e] = Elem<T>::one(q + e) * scale;
+  int lo_min = min(lo_a, lo_b);
+  for (int o = 16; o > 0; o >>= 1) lo_min = min(lo_min, __shfl_xor_sync(FULL, lo_min, o));
+  if (lane == 0) lo_warp[warp] = valid ? lo_min : p.pos;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&full[0]), 1);
+    mbar_init(smem_u32(&full[1]), 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
 
-  // this split's share of the envelope [lo_min, pos]
-  const int env = p.pos - lo_min + 1;
+  // this CTA's share of the union of its heads' envelopes
+  int lo_cta = p.pos;
+  for (int w = 0; w < p.heads; ++w) lo_cta = min(lo_cta, lo_warp[w]);
+  const int env = p.pos - lo_cta + 1;
   const int len = (env + p.splits - 1) / p.splits;
-  const int j_begin = lo_min + split * len;
+  const int j_begin = lo_cta + split * len;
   const int j_end = min(p.pos + 1, j_begin + len);
-
-  const T* Kh = static_cast<const T*>(p.K) + ((int64_t)b * p.Hkv + kvh) * p.n * D;
-  const int sl = lane % S8, rg = lane / S8;
-  const T* Vh = static_cast<const T*>(p.V) + ((int64_t)b * p.Hkv + kvh) * p.n * D + sl * 8;
-  float m = -INFINITY, l = 0.f;
-  float acc[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-  for (int j0 = j_begin; j0 < j_end; j0 += kBlockKeys) {
-    const int cnt = min(kBlockKeys, j_end - j0);
-    // scores of keys j0 + lane and j0 + lane + 32, the multiplicity folded
-    // into the exponent: c_j 2^x = 2^(x + log2 c_j), c_j >= 1 in the envelope
-    float x[2];
-#pragma unroll 1
-    for (int u = 0; u < 2; ++u) {
-      const int jj = lane + 32 * u;
-      x[u] = -INFINITY;
-      if (jj < cnt) {
-        const int j = j0 + jj;
-        int c = 0;
-        for (int t = 0; t < p.s; ++t) c += los[t] <= j ? 1 : 0;
-        x[u] = row_dot<T, D>(qs, Kh + (int64_t)j * D) + __log2f((float)c);
-      }
+  const int nblk = j_begin < j_end ? (j_end - j_begin + C::kKeys - 1) / C::kKeys : 0;
+  const uint8_t* Kg = static_cast<const uint8_t*>(p.K) +
+                      ((int64_t)b * p.Hkv + g) * p.n * C::kRowBytes;
+  const uint8_t* Vg = static_cast<const uint8_t*>(p.V) +
+                      ((int64_t)b * p.Hkv + g) * p.n * C::kRowBytes;
+  const uint32_t sK = smem_u32(smem), sV = sK + 2 * C::kKStage;
+  // block blk into stage blk & 1, issued by warp 0: lane 0 posts the bytes,
+  // then every lane copies its share of the key rows
+  auto issue = [&](int blk) {
+    const int j0 = j_begin + blk * C::kKeys;
+    const int cnt = min(C::kKeys, j_end - j0);
+    const uint32_t bytes = (uint32_t)(cnt * C::kRowBytes);
+    const uint32_t st = (uint32_t)(blk & 1);
+    const uint32_t fb = smem_u32(&full[st]);
+    if (lane == 0) {
+      mbar_arrive_expect_tx(fb, 2 * bytes);
+      bulk_load(sV + st * kStageBytes, Vg + (int64_t)j0 * C::kRowBytes, bytes, fb);
     }
-    const float m_new = fmaxf(m, warp_max(fmaxf(x[0], x[1])));
-    const float f = exp2f(m - m_new);        // 0 on the first block (m = -inf)
-    const float p0 = exp2f(x[0] - m_new), p1 = exp2f(x[1] - m_new);
-    l = l * f + warp_sum(p0 + p1);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] *= f;
-    ps[lane] = p0;
-    ps[lane + 32] = p1;
     __syncwarp();
-    // P V over the block's rows, R rows per warp-wide load, U loads in flight
-    constexpr int U = sizeof(T) == 2 ? 8 : 4;
-    for (int r0 = rg; r0 < cnt; r0 += U * R) {
-      typename Vec<T>::Raw v[U];
+    for (int r = lane; r < cnt; r += 32)
+      bulk_load(sK + st * C::kKStage + (uint32_t)r * C::kKStride,
+                Kg + (int64_t)(j0 + r) * C::kRowBytes, C::kRowBytes, fb);
+  };
+  int issued = 0;
+  if (warp == 0) {
+    for (; issued < 2 && issued < nblk; ++issued) issue(issued);
+  }
+
+  float m = -INFINITY, l = 0.f;
+  float acc[C::kPV];
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int rr = r0 + u * R;
-        if (rr < cnt) v[u] = Vec<T>::raw(Vh + (int64_t)(j0 + rr) * D);
-      }
+  for (int e = 0; e < C::kPV; ++e) acc[e] = 0.f;
+  bool ok = true;
+  int blk = 0;
+  for (; blk < nblk; ++blk) {
+    const uint32_t st = (uint32_t)(blk & 1);
+    const bool got = mbar_wait(smem_u32(&full[st]), (uint32_t)(blk >> 1) & 1u, no_abort, p.wait_ns);
+    ok = __syncthreads_and(got) != 0;
+    if (!ok) break;
+    const int j0 = j_begin + blk * C::kKeys;
+    const int cnt = min(C::kKeys, j_end - j0);
+    const uint32_t kst = sK + st * C::kKStage;
+    const uint8_t* vst = smem + 2 * C::kKStage + st * kStageBytes;
+    if (valid) {
+      // scores of keys j0 + lane + 32 u, the multiplicity folded into the
+      // exponent: c_j 2^x = 2^(x + log2 c_j); c_j = 0 outside this head's
+      // envelope
+      float x[C::kKeys / 32];
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int rr = r0 + u * R;
-        if (rr < cnt) {
-          const float w = ps[rr];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) acc[e] = fmaf(w, Vec<T>::elem(v[u], e), acc[e]);
+      for (int u = 0; u < C::kKeys / 32; ++u) {
+        const int jj = lane + 32 * u;
+        x[u] = -INFINITY;
+        if (jj < cnt) {
+          const int j = j0 + jj;
+          int c = 0;
+          for (int t = 0; t < p.s; ++t) c += los[t] <= j ? 1 : 0;
+          if (c > 0) {
+            const uint32_t krow = kst + (uint32_t)jj * C::kKStride;
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll 4
+            for (int k = 0; k < C::kChunks; ++k) {
+              const uint4 kv = ld_shared_v4(krow + (uint32_t)k * 16u);
+              const float* qq = qs + k * C::kE;
+              if constexpr (sizeof(T) == 2) {
+                a0 = fmaf(qq[0], lo16(kv.x), a0);
+                a1 = fmaf(qq[1], hi16(kv.x), a1);
+                a0 = fmaf(qq[2], lo16(kv.y), a0);
+                a1 = fmaf(qq[3], hi16(kv.y), a1);
+                a0 = fmaf(qq[4], lo16(kv.z), a0);
+                a1 = fmaf(qq[5], hi16(kv.z), a1);
+                a0 = fmaf(qq[6], lo16(kv.w), a0);
+                a1 = fmaf(qq[7], hi16(kv.w), a1);
+              } else {
+                a0 = fmaf(qq[0], __uint_as_float(kv.x), a0);
+                a1 = fmaf(qq[1], __uint_as_float(kv.y), a1);
+                a0 = fmaf(qq[2], __uint_as_float(kv.z), a0);
+                a1 = fmaf(qq[3], __uint_as_float(kv.w), a1);
+              }
+            }
+            x[u] = a0 + a1 + __log2f((float)c);
+          }
         }
       }
+      float mx = x[0];
+#pragma unroll
+      for (int u = 1; u < C::kKeys / 32; ++u) mx = fmaxf(mx, x[u]);
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, o));
+      const float m_new = fmaxf(m, mx);
+      if (m_new > -INFINITY) {
+        const float f = exp2f(m - m_new);        // 0 while m = -inf
+        float sum = 0.f;
+#pragma unroll
+        for (int u = 0; u < C::kKeys / 32; ++u) {
+          const float pu = exp2f(x[u] - m_new);
+          ps[lane + 32 * u] = pu;
+          sum += pu;
+        }
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(FULL, sum, o);
+        l = l * f + sum;
+#pragma unroll
+        for (int e = 0; e < C::kPV; ++e) acc[e] *= f;
+        m = m_new;
+        __syncwarp();
+        // P V: lane takes values lane * kPV .. of every row of the block
+        const uint8_t* vcol = vst + lane * C::kPV * (int)sizeof(T);
+#pragma unroll 4
+        for (int jj = 0; jj < cnt; ++jj) {
+          const float w = ps[jj];
+          const uint8_t* vr = vcol + jj * C::kRowBytes;
+          if constexpr (sizeof(T) == 2 && C::kPV == 4) {
+            const uint2 v2 = *reinterpret_cast<const uint2*>(vr);
+            acc[0] = fmaf(w, lo16(v2.x), acc[0]);
+            acc[1] = fmaf(w, hi16(v2.x), acc[1]);
+            acc[2] = fmaf(w, lo16(v2.y), acc[2]);
+            acc[3] = fmaf(w, hi16(v2.y), acc[3]);
+          } else if constexpr (sizeof(T) == 2) {
+            const uint32_t v1 = *reinterpret_cast<const uint32_t*>(vr);
+            acc[0] = fmaf(w, lo16(v1), acc[0]);
+            acc[1] = fmaf(w, hi16(v1), acc[1]);
+          } else {
+            const float* vf = reinterpret_cast<const float*>(vr);
+#pragma unroll
+            for (int e = 0; e < C::kPV; ++e) acc[e] = fmaf(w, vf[e], acc[e]);
+          }
+        }
+        __syncwarp();   // ps is rewritten by the next block
+      }
     }
-    m = m_new;
-    __syncwarp();   // ps is rewritten by the next block
+    // every warp is done with this stage: refill it with the block after next
+    __syncthreads();
+    if (warp == 0 && issued < nblk) {
+      issue(issued);
+      ++issued;
+    }
   }
-  // lanes holding the same slice of different rows add up
-#pragma unroll
-  for (int o = S8; o < 32; o <<= 1)
-#pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
-  if (rg == 0) {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) p.part_o[(int64_t)item * D + sl * 8 + e] = acc[e];
+  if (!ok) {
+    // let the copies issued and not yet waited for land before the CTA's
+    // memory goes away
+    if (warp == 0) {
+      for (int k = blk; k < issued; ++k)
+        mbar_wait(smem_u32(&full[k & 1]), (uint32_t)(k >> 1) & 1u, no_abort, p.wait_ns);
+      if (lane == 0) atomicOr(p.err, 1);
+    }
+    return;
   }
-  if (lane == 0) {
-    p.part_m[item] = m;    // -inf and 0 for a split past the envelope
-    p.part_l[item] = l;
+  if (valid) {
+    const int64_t item = ((int64_t)b * p.Hq + h) * p.splits + split;
+#pragma unroll
+    for (int e = 0; e < C::kPV; ++e) p.part_o[item * D + lane * C::kPV + e] = acc[e];
+    if (lane == 0) {
+      p.part_m[item] = m;    // -inf and 0 for a share with no key of this head
+      p.part_l[item] = l;
+    }
   }
 }
 
-// O = sum_k 2^(m_k - m) P V_k / sum_k 2^(m_k - m) l_k over the non-empty splits
+// O = sum_k 2^(m_k - m) P V_k / sum_k 2^(m_k - m) l_k over the non-empty shares
 template <typename T, int D>
 __global__ void __launch_bounds__(D)
 decode_merge_kernel(DecodeParams p, void* out) {
   const int bh = blockIdx.x, e = threadIdx.x;
   const int64_t first = (int64_t)bh * p.splits;
   float m = -INFINITY;
-  for (int k = 0; k < p.splits; ++k) m = fmaxf(m, p.part_m[first + k]);
+  for (int k = 0; k < p.splits; ++k)
+    if (p.part_l[first + k] > 0.f) m = fmaxf(m, p.part_m[first + k]);
   float l = 0.f, o = 0.f;
   for (int k = 0; k < p.splits; ++k) {
-    if (p.part_l[first + k] == 0.f) continue;
+    if (!(p.part_l[first + k] > 0.f)) continue;
     const float f = exp2f(p.part_m[first + k] - m);
     l = fmaf(f, p.part_l[first + k], l);
     o = fmaf(f, p.part_o[(first + k) * D + e], o);
   }
-  Vec<T>::store(static_cast<T*>(out) + (int64_t)bh * D + e, o / l);
+  Elem<T>::store(static_cast<T*>(out) + (int64_t)bh * D + e, o / l);
 }
 
 template <typename T, int D>
 cudaError_t launch_typed(const DecodeParams& p, void* out, cudaStream_t st) {
-  const int64_t warps = (int64_t)p.B * p.Hq * p.splits;
-  decode_partial_kernel<T, D><<<(unsigned)((warps + kWarps - 1) / kWarps), kThreads, 0, st>>>(p);
+  using C = Cfg<T, D>;
+  auto kern = decode_group_kernel<T, D>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)C::kSmem);
+  if (e != cudaSuccess) return e;
+  const int64_t ctas = (int64_t)p.B * p.Hkv * p.hchunks * p.splits;
+  kern<<<(unsigned)ctas, 32 * p.heads, C::kSmem, st>>>(p);
   decode_merge_kernel<T, D><<<(unsigned)(p.B * p.Hq), D, 0, st>>>(p, out);
   return cudaGetLastError();
 }
@@ -263,10 +351,14 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
   p.s = a.s;
   p.W = a.W;
   p.pos = a.pos;
-  p.splits = decode_splits(a.B, a.Hq, a.num_sms);
+  p.heads = decode_heads(a.Hq / a.Hkv);
+  p.hchunks = (a.Hq / a.Hkv + p.heads - 1) / p.heads;
+  p.splits = decode_splits(a.B, a.Hq, a.Hkv, a.num_sms);
   p.part_m = a.work;
   p.part_l = a.work + (size_t)a.B * a.Hq * p.splits;
   p.part_o = a.work + 2 * (size_t)a.B * a.Hq * p.splits;
+  p.err = a.err;
+  p.wait_ns = a.wait_ns;
   if (a.dtype == PLSH_BF16)
     return a.d == 64 ? launch_typed<__nv_bfloat16, 64>(p, a.o, st)
                      : launch_typed<__nv_bfloat16, 128>(p, a.o, st);

@@ -27,12 +27,27 @@ constexpr int kMaxExactHeads = 512;
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 
 // Work-item table of the tensor-core kernel for one problem shape and head
-// order, kept on the device once built.
+// order, kept on the device once built.  Items whose key envelope is long are
+// split into parts over the key range: each part has an entry in `ext`
+// {part, parts, workspace slot, 0} (no `ext` when nothing is split), writes
+// its partial rows (unnormalised P V, max, row sum) to its workspace slot, and
+// `merge` lists the split items {b, hA | hB << 16, qtA, qtB}, {first slot,
+// parts, 0, 0} for the kernel that combines the parts into O.
 struct ItemTable {
   std::vector<int4> host;
+  std::vector<int4> ext;
+  std::vector<int4> merge;
   int4* dev = nullptr;
+  int4* dev_ext = nullptr;
+  int4* dev_merge = nullptr;
+  float* ws = nullptr;
   uint64_t last_use = 0;
 };
+// floats of one split part's workspace slot: both tiles' rows of P V, then
+// their maxima, then their row sums
+constexpr int kSplitRowFloats = 128;
+constexpr size_t kSplitSlotFloats = 2 * 128 * (kSplitRowFloats + 2);
+constexpr int kMaxSplitParts = 16;
 
 // Per-device library state.
 constexpr int kMaxHostChunks = 4;    // query-row chunks of the host-buffer entry point
@@ -40,6 +55,7 @@ struct DeviceCtx {
   int device = -1;
   int num_sms = 0;
   int* d_err = nullptr;        // device error flag (bit 0: wait timeout)
+  int split_parts = 0;         // 0: automatic, 1: never split, >= 2: every item in that many parts
   int* d_queue = nullptr;      // kQueueSlots x {next item, finished CTAs}
   uint64_t slot_counter = 0;
   uint64_t wait_ns = kDefaultWaitNs;
@@ -99,22 +115,28 @@ struct AttnArgs {
   // one KV head, {b, hA | hB << 16, qtA, qtB (-1: none)}, in cost order
   const int4* items;
   int num_items;
+  const int4* item_ext;            // split parts {part, parts, slot, 0}, or null
+  float* split_ws;                 // workspace slots of split parts
   int* err;
   int* queue;                      // {next item, finished CTAs}
   uint64_t wait_ns;
   int stall;                       // fault injection: the scheduler publishes no item
 };
 
-// decode.cu: one query position against the cached keys; each (batch
-// element, head) is split S ways over its key envelope, a warp per split,
-// S chosen for about 64 warps per SM in all (at most 64 splits)
-inline int decode_splits(int B, int Hq, int num_sms) {
-  const int64_t bh = (int64_t)B * Hq, want = (int64_t)num_sms * 64;
-  const int64_t sp = (want + bh - 1) / bh;
+// decode.cu: one query position against the cached keys.  A CTA serves up
+// to eight query heads of one KV group (a warp each) over one of S shares of
+// the union of their key envelopes; S is chosen for about three CTAs per SM
+// (at most 64).
+inline int decode_heads(int G) { return G < 8 ? G : 8; }
+inline int decode_splits(int B, int Hq, int Hkv, int num_sms) {
+  const int G = Hq / Hkv;
+  const int64_t ctas = (int64_t)B * Hkv * ((G + decode_heads(G) - 1) / decode_heads(G));
+  const int64_t want = 12LL * num_sms;
+  const int64_t sp = (want + ctas - 1) / ctas;
   return (int)(sp < 1 ? 1 : (sp > 64 ? 64 : sp));
 }
-inline size_t decode_work_floats(int B, int Hq, int d, int num_sms) {
-  return (size_t)B * Hq * decode_splits(B, Hq, num_sms) * (size_t)(d + 2);
+inline size_t decode_work_floats(int B, int Hq, int Hkv, int d, int num_sms) {
+  return (size_t)B * Hq * decode_splits(B, Hq, Hkv, num_sms) * (size_t)(d + 2);
 }
 struct DecodeArgs {
   const void* q;         // [B, Hq, 1, d]
@@ -127,7 +149,9 @@ struct DecodeArgs {
   int pos;
   int dtype;             // PLSH_BF16 or PLSH_F32
   int num_sms;
-  float* work;           // decode_work_floats(B, Hq, d, pos)
+  float* work;           // decode_work_floats(B, Hq, Hkv, d, num_sms)
+  int* err;              // device error flag (bit 0: a bounded wait ran out)
+  uint64_t wait_ns;
 };
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
 
@@ -138,6 +162,10 @@ cudaError_t launch_attn_simt(const AttnArgs& a, const float* slopes_host,
 // attn_tc.cu (tcgen05 tensor cores, bf16, d = 128)
 cudaError_t launch_attn_tc(const AttnArgs& a, const float* slopes_host,
                            int num_sms, cudaStream_t st);
+// combines the parts of `count` split items (entries of `merge`, two int4
+// each) into O (bf16 [B, Hq, n, 128])
+cudaError_t launch_split_merge(const int4* merge, int count, const float* ws, void* O, int Hq,
+                               int n, cudaStream_t st);
 size_t attn_tc_smem_bytes(int s, int causal, int exact);
 
 }  // namespace plsh

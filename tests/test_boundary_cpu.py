@@ -171,3 +171,8 @@ def test_attn_path_query(lib):
     assert path(plsh.PLSH_BF16, 64) == plsh.PLSH_PATH_CUDA_CORES
     assert path(plsh.PLSH_F32, 128) == plsh.PLSH_PATH_CUDA_CORES
     assert lib.plsh_attn_path(None, None, 1, ctypes.byref(out)) == plsh.PLSH_ERR_INVALID
+
+
+def test_split_parts_setting_is_validated(lib):
+    assert lib.plsh_set_split_parts(-1) == plsh.PLSH_ERR_INVALID
+    assert lib.plsh_set_split_parts(17) == plsh.PLSH_ERR_INVALID

@@ -335,3 +335,65 @@ def test_v_beyond_f16_range_is_reported(exact):
     assert err.value.status == plsh.PLSH_ERR_RANGE
     plsh.stream_status()
     bins.free()
+
+
+# ---------------------------------------- key-range split of long items
+SPLIT_CASES = [
+    # name, B, Hq, Hkv, n, d, causal, s, sigma
+    ("causal_ragged", 1, 4, 2, 1000, 128, True, 10, (1.2, 6.0, 40.0, 300.0)),
+    ("noncausal", 2, 2, 1, 777, 128, False, 6, (3.0, 150.0)),
+    ("odd_group", 1, 3, 1, 900, 128, True, 7, (2.5, 90.0, 400.0)),
+    ("sorted_lists", 1, 2, 1, 700, 128, True, 24, (3.0, 50.0)),
+]
+
+
+@pytest.mark.parametrize("parts", [2, 3])
+@pytest.mark.parametrize("case", SPLIT_CASES, ids=[c[0] for c in SPLIT_CASES])
+def test_forced_split_all_rows(case, parts):
+    """Every work item cut into 2 or 3 key ranges (parts past an item's
+    envelope do nothing), partial rows combined by the merge kernel: every
+    row against the oracle, approximation and exact ALiBi."""
+    name, B, Hq, Hkv, n, d, causal, s, sig = case
+    w = Workload(name, B, Hq, Hkv, n, d, "bf16", causal, s, sig, qkv_seed=n + parts)
+    Q, K, V = make_qkv(w)
+    sigma = w.sigmas()
+    bins = plsh.sample_bins(n, sigma, s, seed=9)
+    off, st = oracle.sample_bins(n, sigma, s, seed=9)
+    rows = oracle.all_rows(B, Hq, n)
+    plsh.set_split_parts(parts)
+    try:
+        O = run_approx(w, Q, K, V, bins)
+        E = plsh.alibi_exact(to_dev(Q, "bf16"), to_dev(K, "bf16"), to_dev(V, "bf16"), sigma,
+                             causal)
+        plsh.stream_status()
+    finally:
+        plsh.set_split_parts(0)
+    ref = oracle.plsh_attn_rows(Q, K, V, off, st, s, causal, rows)
+    assert_close(gather_rows(O, rows), ref, "bf16", f"split {parts} {name}")
+    ref_e = oracle.alibi_exact_rows(Q, K, V, sigma, causal, rows)
+    assert_close(gather_rows(E, rows), ref_e, "bf16", f"split {parts} exact {name}")
+    bins.free()
+
+
+def test_automatic_split_long_envelopes():
+    """One pair of heads whose bins span thousands of keys: the automatic
+    split cuts the long items of the last row tiles; every row of both heads
+    against the oracle, and against the unsplit kernel."""
+    n, s = 4096, 6
+    w = Workload("long", 1, 2, 1, n, 128, "bf16", True, s, (3000.0, 4000.0), qkv_seed=21)
+    Q, K, V = make_qkv(w)
+    sigma = w.sigmas()
+    bins = plsh.sample_bins(n, sigma, s, seed=2)
+    off, st = oracle.sample_bins(n, sigma, s, seed=2)
+    plsh.set_split_parts(0)
+    O = run_approx(w, Q, K, V, bins)
+    plsh.set_split_parts(1)
+    try:
+        O1 = run_approx(w, Q, K, V, bins)
+    finally:
+        plsh.set_split_parts(0)
+    rows = oracle.all_rows(1, 2, n)
+    ref = oracle.plsh_attn_rows(Q, K, V, off, st, s, True, rows)
+    assert_close(gather_rows(O, rows), ref, "bf16", "automatic split")
+    assert_close(gather_rows(O1, rows), ref, "bf16", "unsplit")
+    bins.free()
