@@ -370,6 +370,7 @@ def run_ours(args, rank, world):
     result["decode"] = measure_decode(w, bins, sigma, flush, stream)
     result["fixed_blocks"] = measure_fixed(w, sigma, Q, K, V, E, flush, stream)
     result["shared_groups"] = measure_shared_groups(w, sigma, Q, K, V, E, flush, stream)
+    result["backward"] = measure_backward(w, bins, Q, K, V, f_block, flush, stream)
     result["bias_error"] = measure_bias_error()
     if not args.no_configs:
         del E
@@ -509,6 +510,36 @@ def measure_crossover(flush, stream, scout=None):
                      "speedup_over_exact": r["exact_ms"] / r["approx_ms"],
                      "approx_error_vs_exact_rel_fro": r["approx_error_vs_exact_rel_fro"]})
     return rows
+
+
+# ------------------------------------------------------------ backward
+def measure_backward(w, bins, Q, K, V, f_block, flush, stream, iters=5):
+    """Gradients of the workload's attention for a random dO: the tensor-core
+    path (a forward pass in its row statistics mode, the backward kernel,
+    the dQ conversion) against its roofline, the paper's block work of the
+    backward (S, dP, dV, dK, dQ: 10 d per block pair, 2.5 x the forward's
+    F_block) at the bf16 peak; and the CUDA-core path on the same call."""
+    import torch
+    import positional_lsh_approximation_gb300 as plsh
+    g = torch.Generator(device=Q.device)
+    g.manual_seed(99)
+    dO = torch.randn(Q.shape, generator=g, device=Q.device).to(Q.dtype)
+    run = lambda: plsh.alibi_attn_backward(Q, K, V, dO, bins, w.causal)
+    t = time_calls(run, flush, stream, iters)
+    plsh.stream_status()
+    os.environ["PLSH_PATH"] = "simt"
+    try:
+        t_simt = time_calls(run, flush, stream, 2)
+    finally:
+        del os.environ["PLSH_PATH"]
+    plsh.stream_status()
+    pk = peaks()
+    f_bwd = 2.5 * f_block
+    return {"path": plsh.attn_path(Q, bins, w.causal), "ms": t,
+            "tokens_per_s": w.B * w.n / (t / 1e3), "flops_per_call": f_bwd,
+            "tensor_frac": f_bwd / (t / 1e3) / 1e12 / pk["bf16_tflops"],
+            "cuda_core_ms": t_simt,
+            "kernels": "attn_tc_kernel (row statistics) + bwd_tc_kernel + dq_convert_kernel"}
 
 
 # ------------------------------------------- hashes shared across a group

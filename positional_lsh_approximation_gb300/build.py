@@ -14,7 +14,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 SRC_DIR = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libplsh.so")
-SOURCES = ["api.cu", "sampler.cu", "attn_simt.cu", "attn_tc.cu", "decode.cu", "bias.cu", "bwd.cu"]
+SOURCES = ["api.cu", "sampler.cu", "attn_simt.cu", "attn_tc.cu", "decode.cu", "bias.cu", "bwd.cu",
+           "bwd_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
          "-Xcompiler", "-ffp-contract=off", "--expt-relaxed-constexpr"]

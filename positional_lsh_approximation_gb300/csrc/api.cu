@@ -355,14 +355,14 @@ void free_table(plsh::ItemTable& t) {
 
 plsh_status item_table(plsh::DeviceCtx* ctx, int B, int Hq, int Hkv, int QT, int qt0, int qt1,
                        bool exact, bool causal, int s, const std::vector<double>& sigma,
-                       cudaStream_t st, TableRef* out) {
+                       int split_parts, cudaStream_t st, TableRef* out) {
   // the table depends on the shape, the range of query tiles, the split
   // setting and, for the approximate kernel, on the order of sigma inside
   // each KV group and across heads (and on s and sigma through the split)
   std::string key = std::to_string(exact) + ":" + std::to_string(causal) + ":" +
                     std::to_string(B) + ":" + std::to_string(Hq) + ":" + std::to_string(Hkv) +
                     ":" + std::to_string(QT) + ":" + std::to_string(qt0) + "-" +
-                    std::to_string(qt1) + ":split" + std::to_string(ctx->split_parts);
+                    std::to_string(qt1) + ":split" + std::to_string(split_parts);
   if (!exact) {
     std::vector<int> rank(Hq);
     std::iota(rank.begin(), rank.end(), 0);
@@ -370,7 +370,7 @@ plsh_status item_table(plsh::DeviceCtx* ctx, int B, int Hq, int Hkv, int QT, int
                      [&](int x, int y) { return sigma[x] > sigma[y]; });
     key += ":s" + std::to_string(s) + ":";
     for (int h : rank) key += std::to_string(h) + ",";
-    if (ctx->split_parts == 0) {
+    if (split_parts == 0) {
       // the automatic split follows the scales themselves
       char buf[32];
       for (double v : sigma) {
@@ -392,7 +392,7 @@ plsh_status item_table(plsh::DeviceCtx* ctx, int B, int Hq, int Hkv, int QT, int
     }
     plsh::ItemTable t;
     ItemList lst = build_items(B, Hq, Hkv, QT, qt0, qt1, exact, causal, s, ctx->num_sms,
-                               ctx->split_parts, sigma);
+                               split_parts, sigma);
     t.host = std::move(lst.items);
     t.ext = std::move(lst.ext);
     t.merge = std::move(lst.merge);
@@ -435,6 +435,17 @@ plsh_status item_table(plsh::DeviceCtx* ctx, int B, int Hq, int Hkv, int QT, int
 }
 
 enum class Path { Auto, Simt, Tc };
+
+Path path_override();
+
+// The tensor-core backward serves bf16 with d = 128, s <= 16 and at most 64
+// query heads per KV head (and a forward statistics pass on the tensor-core
+// kernel); everything else takes the CUDA-core backward.
+bool bwd_tc_ok(const plsh_tensor* Q, const plsh_tensor* K, const plsh_bins* bins, int causal) {
+  return path_override() != Path::Simt && Q->dtype == PLSH_BF16 && Q->d == 128 &&
+         bins->s <= plsh::kBwdTcMaxS && Q->H / K->H <= plsh::kBwdTcMaxGroup &&
+         plsh::attn_tc_smem_bytes(bins->s, causal, 0) <= 232448;
+}
 
 // The tensor-core kernel serves bf16 with d = 128 and s within its shared
 // memory; everything else takes the CUDA-core kernel.
@@ -503,7 +514,8 @@ plsh_status run_attention(const plsh_tensor* Q, const plsh_tensor* K, const plsh
     const int QT = (int)((Q->n + 127) / 128);
     plsh_status s1 = item_table(ctx, a.B, a.Hq, a.Hkv, QT, qt0, qt1 < 0 ? QT : qt1, a.exact != 0,
                                 a.causal != 0, a.s,
-                                bins ? bins->sigma_host : std::vector<double>(), st, &tab);
+                                bins ? bins->sigma_host : std::vector<double>(),
+                                ctx->split_parts, st, &tab);
     if (s1 != PLSH_OK) return s1;
     a.items = tab.items;
     a.num_items = tab.count;
@@ -748,6 +760,66 @@ plsh_status plsh_alibi_attn_backward(const plsh_tensor* Q, const plsh_tensor* K,
   cudaStream_t cs = (cudaStream_t)stream;
   float* stats = nullptr;
   const size_t bytes = sizeof(float) * 3 * (size_t)Q->B * Q->H * Q->n;
+  if (bwd_tc_ok(Q, K, bins, causal ? 1 : 0)) {
+    // tensor cores: the forward kernel in its row statistics mode (m, l and
+    // Delta = dO . O per row, no output), then the backward kernel
+    plsh::DeviceCtx* ctx = nullptr;
+    if ((st = current_ctx(&ctx)) != PLSH_OK) return st;
+    float* dq_acc = nullptr;
+    const size_t acc_bytes = sizeof(float) * (size_t)Q->B * Q->H * Q->n * Q->d;
+    PLSH_TRY_CUDA(cudaMallocAsync((void**)&stats, bytes, cs), "backward scratch");
+    cudaError_t e = cudaMallocAsync((void**)&dq_acc, acc_bytes, cs);
+    if (e != cudaSuccess) {
+      cudaFreeAsync(stats, cs);
+      return cuda_fail(e, "backward scratch");
+    }
+    plsh::AttnArgs a;
+    memset(&a, 0, sizeof a);
+    a.Q = Q->data;
+    a.K = K->data;
+    a.V = V->data;
+    a.O = nullptr;
+    a.B = (int)Q->B;
+    a.Hq = (int)Q->H;
+    a.Hkv = (int)K->H;
+    a.n = (int)Q->n;
+    a.d = (int)Q->d;
+    a.causal = causal ? 1 : 0;
+    a.rec = bins->d_rec;
+    a.s = bins->s;
+    a.W = bins->W;
+    a.err = ctx->d_err;
+    a.wait_ns = ctx->wait_ns;
+    a.stats = stats;
+    a.dO = dO->data;
+    {
+      std::lock_guard<std::mutex> lk(g_ctx_mu);
+      a.queue = ctx->d_queue + 2 * (ctx->slot_counter++ % plsh::kQueueSlots);
+    }
+    int* bq = nullptr;
+    {
+      std::lock_guard<std::mutex> lk(g_ctx_mu);
+      bq = ctx->d_queue + 2 * (ctx->slot_counter++ % plsh::kQueueSlots);
+    }
+    const int QT = (int)((Q->n + 127) / 128);
+    TableRef tab;
+    plsh_status s1 = item_table(ctx, a.B, a.Hq, a.Hkv, QT, 0, QT, false, a.causal != 0, a.s,
+                                bins->sigma_host, 1, cs, &tab);
+    if (s1 == PLSH_OK) {
+      a.items = tab.items;
+      a.num_items = tab.count;
+      e = plsh::launch_attn_tc(a, nullptr, ctx->num_sms, cs);
+      if (e == cudaSuccess)
+        e = plsh::launch_attn_bwd_tc(Q->data, K->data, V->data, dO->data, dQ->data, dK->data,
+                                     dV->data, stats, dq_acc, bins, a.B, a.Hq, a.Hkv, a.n,
+                                     a.causal, bq, ctx->d_err, ctx->wait_ns, ctx->num_sms, cs);
+    }
+    const cudaError_t f1 = cudaFreeAsync(stats, cs), f2 = cudaFreeAsync(dq_acc, cs);
+    if (s1 != PLSH_OK) return s1;
+    if (e == cudaSuccess) e = f1 != cudaSuccess ? f1 : f2;
+    PLSH_TRY_CUDA(e, "backward launch");
+    return PLSH_OK;
+  }
   PLSH_TRY_CUDA(cudaMallocAsync((void**)&stats, bytes, cs), "backward scratch");
   cudaError_t e = plsh::launch_attn_bwd(Q->data, K->data, V->data, dO->data, dQ->data, dK->data,
                                         dV->data, stats, bins, (int)Q->B, (int)Q->H, (int)K->H,

@@ -755,6 +755,45 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         return true;
       }
       const float inv_l = pend_l > 0.f ? 1.f / pend_l : 0.f;
+      if (a.stats != nullptr) {
+        // m, l and Delta = sum_d (acc_d / l) dO_d for the backward pass (the
+        // TMEM loads are warp-wide: every lane takes part, valid rows or not)
+        const bool valid = qt >= 0 && i < n;
+        const uint4* dorow = reinterpret_cast<const uint4*>(
+            static_cast<const uint16_t*>(a.dO) + (row0 + (valid ? i : 0)) * HD);
+        float dsum = 0.f;
+#pragma unroll 1
+        for (int q2 = 0; q2 < 4; ++q2) {
+          uint32_t o[32];
+          tmem_ld32(o_col + q2 * 32, o);
+          tmem_wait_ld();
+          if (valid) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const uint4 g = dorow[q2 * 4 + v];
+              const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                dsum = fmaf(__uint_as_float(o[8 * v + 2 * k]), __uint_as_float(gw[k] << 16), dsum);
+                dsum = fmaf(__uint_as_float(o[8 * v + 2 * k + 1]),
+                            __uint_as_float(gw[k] & 0xffff0000u), dsum);
+              }
+            }
+          }
+        }
+        if (valid) {
+          float* st3 = a.stats + (row0 + i) * 3;
+          st3[0] = pend_m;
+          st3[1] = pend_l;
+          st3[2] = dsum * inv_l;
+        }
+        if (a.O == nullptr) {
+          tc_fence_before();
+          mbar_arrive(bar(B_IEMPTY + pslot));
+          pend = false;
+          return true;
+        }
+      }
 #pragma unroll 1
       for (int q2 = 0; q2 < 2; ++q2) {
         uint32_t o0[32], o1[32];
@@ -1429,6 +1468,10 @@ bool out_staged(int s, int causal, int exact) {
   return smem_for(kSlots, true, s, causal, exact) <= kSmemLimit;
 }
 }  // namespace
+
+bool make_tile_map_bf16(CUtensorMap* map, const void* base, int64_t planes, int64_t n) {
+  return make_map(map, base, planes, n, BM);
+}
 
 size_t attn_tc_smem_bytes(int s, int causal, int exact) {
   return smem_for(kSlots, out_staged(s, causal, exact), s, causal, exact);

@@ -1,6 +1,8 @@
 """GPU checks of plsh_alibi_attn_backward against the oracle's gradients.
 fp32 inputs: 1e-4 relative to the largest gradient entry; bf16 inputs: the
-gradients are rounded to bf16, 1e-2 of that scale."""
+gradients are rounded to bf16, 1e-2 of that scale.  bf16 with d = 128 and
+s <= 16 runs on the tensor cores (P and dS in bf16), everything else on the
+CUDA cores."""
 import numpy as np
 import pytest
 import torch
@@ -26,6 +28,12 @@ CASES = [
     ("f32_noncausal", 1, 2, 1, 300, 64, "f32", False, 6, (2.0, 40.0)),
     ("bf16_causal", 1, 4, 2, 400, 128, "bf16", True, 10, (1.2, 6.0, 40.0, 300.0)),
     ("bf16_noncausal_d64", 1, 2, 2, 333, 64, "bf16", False, 4, (5.0, 60.0)),
+    # tensor-core path: several key tiles, ragged tails, GQA, s = 16
+    ("tc_noncausal", 2, 4, 1, 520, 128, "bf16", False, 6, (3.0, 25.0, 150.0, 900.0)),
+    ("tc_causal_gqa4", 1, 8, 2, 1000, 128, "bf16", True, 10,
+     (1.2, 6.0, 40.0, 300.0, 2.0, 9.0, 70.0, 500.0)),
+    ("tc_causal_s16", 1, 2, 1, 700, 128, "bf16", True, 16, (4.0, 120.0)),
+    ("tc_one_tile", 1, 2, 2, 100, 128, "bf16", True, 3, (2.0, 1e4)),
 ]
 
 
@@ -51,4 +59,26 @@ def test_backward_matches_oracle(case):
         scale = np.abs(want).max()
         err = np.abs(g - want).max()
         assert err <= rel * scale, f"{name} {what}: max err {err:.3e} vs scale {scale:.3e}"
+    bins.free()
+
+
+def test_tensor_core_backward_agrees_with_cuda_cores(monkeypatch):
+    """The same gradients from both kernels (bf16 outputs), a causal GQA case
+    over several key tiles."""
+    w = Workload("agree", 1, 4, 2, 600, 128, "bf16", True, 8, (2.0, 10.0, 60.0, 400.0),
+                 qkv_seed=77)
+    Q, K, V = make_qkv(w)
+    dO = np.random.default_rng(5).standard_normal(Q.shape).astype(np.float32)
+    dev = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(torch.bfloat16).cuda()
+    bins = plsh.sample_bins(w.n, w.sigmas(), w.s, seed=4)
+    tc = plsh.alibi_attn_backward(dev(Q), dev(K), dev(V), dev(dO), bins, True)
+    plsh.stream_status()
+    monkeypatch.setenv("PLSH_PATH", "simt")
+    simt = plsh.alibi_attn_backward(dev(Q), dev(K), dev(V), dev(dO), bins, True)
+    plsh.stream_status()
+    for a, b, what in zip(tc, simt, ("dQ", "dK", "dV")):
+        a = a.float().cpu().numpy()
+        b = b.float().cpu().numpy()
+        scale = np.abs(b).max()
+        assert np.abs(a - b).max() <= 1.5e-2 * scale, what
     bins.free()
