@@ -677,7 +677,7 @@ def measure_decode(w, bins, sigma, flush, stream, iters=20):
             "envelope_keys_mean": float(np.mean(env)), "bytes": bytes_,
             "achieved_gbs": bytes_ / t / 1e9, "peak_gbs": pk["hbm_gbs"],
             "hbm_frac": bytes_ / t / 1e9 / pk["hbm_gbs"], "peak_source": pk["source"],
-            "kernels": "decode_partial_kernel + decode_merge_kernel",
+            "kernels": "decode_group_kernel + decode_merge_kernel",
             "l2": "evicted before each step (256 MiB read)"}
 
 
