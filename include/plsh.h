@@ -142,10 +142,20 @@ plsh_status plsh_bins_fixed(int64_t n, const int32_t* width_h, int32_t H, int32_
  * a KV head collecting the sums of every query head that reads it.
  *   Q, dO, dQ [B,Hq,n,d]; K, V, dK, dV [B,Hkv,n,d]; one dtype (PLSH_BF16 or
  *   PLSH_F32), d in {64, 128}; bins and causal as for plsh_alibi_attn.
- * CUDA cores, fp32 accumulation, no atomics: a warp per row computes the
- * row's max, sum and sum_j P_ij dP_ij (kept in stream-ordered scratch of
- * 3 B Hq n floats) and dQ_i; a warp per key then sums dK_j and dV_j over the
- * rows whose bins contain it.  Asynchronous on `stream`.
+ * Tensor cores (bf16, d = 128, s <= 16, Hq / Hkv <= 64; plsh_attn_path names
+ * the path): the forward kernel in a row statistics mode writes each row's
+ * max, sum and Delta_i = dO_i . O_i, then a kernel per (batch, KV head, key
+ * tile) forms S^T, dP^T, dV, dK and dS K with tcgen05 products (P and dS
+ * rounded to bf16, fp32 accumulation), the dS K rows added to an fp32 dQ
+ * accumulator by TMA reductions and converted to bf16 at the end.
+ * CUDA cores (every other case), fp32 accumulation, no atomics: a warp per
+ * row computes the row's max, sum and sum_j P_ij dP_ij and dQ_i; a warp per
+ * key then sums dK_j and dV_j over the rows whose bins contain it.
+ * Scratch (3 B Hq n floats of row statistics, plus B Hq n d floats of dQ
+ * accumulator on the tensor cores) lives in a device buffer the library
+ * keeps per device between calls, grown on demand (which synchronises the
+ * device); calls on different streams are ordered on it by an event.
+ * Asynchronous on `stream`.
  */
 plsh_status plsh_alibi_attn_backward(const plsh_tensor* Q, const plsh_tensor* K,
                                      const plsh_tensor* V, const plsh_tensor* dO,
@@ -330,10 +340,13 @@ plsh_status plsh_alibi_exact(const plsh_tensor* Q, const plsh_tensor* K,
  *   K, V [B,Hkv,n,d]: the cache; rows above pos are not read.
  *   All the same dtype (PLSH_BF16 or PLSH_F32), d in {64, 128}, Hq % Hkv == 0,
  *   B * Hq <= 65535, bins->n == n, bins->H == Hq, 0 <= pos < n.
- * The key envelope is split into chunks of 512 keys whose partial results
- * (max, row sum, unnormalised P V) are merged into o; the partials live in a
- * device buffer the library keeps per device (B * Hq * (pos/512 + 1) *
- * (d + 2) floats, grown on demand, which synchronises the device).
+ * A CTA serves the query heads of one KV group (up to 8) over one share of
+ * the union of their envelopes; the shares' partial results (max, row sum,
+ * unnormalised P V) are merged into o.  The partials live in a device buffer
+ * the library keeps per device (B * Hq * S * (d + 2) floats, S <= 64 shares
+ * chosen so that about 12 CTAs per SM run; grown on demand, which
+ * synchronises the device; calls on different streams are ordered on it by
+ * an event).
  * Asynchronous on `stream`; errors in the arguments return before any launch.
  */
 plsh_status plsh_alibi_decode(const plsh_tensor* q, const plsh_tensor* K,

@@ -36,6 +36,31 @@ plsh_status cuda_fail(cudaError_t e, const char* what) {
 
 constexpr int kMaxDevices = 64;
 std::mutex g_ctx_mu;
+// held while a call enqueues work on a per-device scratch buffer
+std::mutex g_bwd_mu, g_decode_mu;
+
+plsh_status dev_alloc(void** p, size_t bytes, const char* what);
+
+// A per-device scratch buffer of at least `bytes`, ordered after its last
+// use on any stream: grown (after a device synchronisation, since earlier
+// calls may still read the old one) when too small; the calling stream
+// waits for the event recorded after the last use.  The caller holds the
+// buffer's mutex and records *ev on its stream after its launches.
+plsh_status scratch_acquire(float** buf, size_t* have, cudaEvent_t* ev, size_t bytes,
+                            cudaStream_t cs, const char* what) {
+  if (*have < bytes) {
+    PLSH_TRY_CUDA(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
+    cudaFree(*buf);
+    *buf = nullptr;
+    *have = 0;
+    plsh_status st = dev_alloc((void**)buf, bytes, what);
+    if (st != PLSH_OK) return st;
+    *have = bytes;
+  }
+  if (*ev == nullptr) PLSH_TRY_CUDA(cudaEventCreateWithFlags(ev, cudaEventDisableTiming), what);
+  PLSH_TRY_CUDA(cudaStreamWaitEvent(cs, *ev, 0), what);
+  return PLSH_OK;
+}
 plsh::DeviceCtx g_ctx[kMaxDevices];
 
 // Fault injection for the tests, from the environment: PLSH_FAULT=oom fails
@@ -765,14 +790,16 @@ plsh_status plsh_alibi_attn_backward(const plsh_tensor* Q, const plsh_tensor* K,
     // Delta = dO . O per row, no output), then the backward kernel
     plsh::DeviceCtx* ctx = nullptr;
     if ((st = current_ctx(&ctx)) != PLSH_OK) return st;
-    float* dq_acc = nullptr;
+    const size_t stat_floats = ((bytes / sizeof(float)) + 63) & ~(size_t)63;
     const size_t acc_bytes = sizeof(float) * (size_t)Q->B * Q->H * Q->n * Q->d;
-    PLSH_TRY_CUDA(cudaMallocAsync((void**)&stats, bytes, cs), "backward scratch");
-    cudaError_t e = cudaMallocAsync((void**)&dq_acc, acc_bytes, cs);
-    if (e != cudaSuccess) {
-      cudaFreeAsync(stats, cs);
-      return cuda_fail(e, "backward scratch");
-    }
+    std::lock_guard<std::mutex> bk(g_bwd_mu);
+    if ((st = scratch_acquire(&ctx->bwd_work, &ctx->bwd_work_bytes, &ctx->bwd_ev,
+                              sizeof(float) * stat_floats + acc_bytes, cs, "backward scratch")) !=
+        PLSH_OK)
+      return st;
+    stats = ctx->bwd_work;
+    float* dq_acc = ctx->bwd_work + stat_floats;
+    cudaError_t e = cudaSuccess;
     plsh::AttnArgs a;
     memset(&a, 0, sizeof a);
     a.Q = Q->data;
@@ -814,18 +841,24 @@ plsh_status plsh_alibi_attn_backward(const plsh_tensor* Q, const plsh_tensor* K,
                                      dV->data, stats, dq_acc, bins, a.B, a.Hq, a.Hkv, a.n,
                                      a.causal, bq, ctx->d_err, ctx->wait_ns, ctx->num_sms, cs);
     }
-    const cudaError_t f1 = cudaFreeAsync(stats, cs), f2 = cudaFreeAsync(dq_acc, cs);
+    const cudaError_t er = cudaEventRecord(ctx->bwd_ev, cs);
     if (s1 != PLSH_OK) return s1;
-    if (e == cudaSuccess) e = f1 != cudaSuccess ? f1 : f2;
+    if (e == cudaSuccess) e = er;
     PLSH_TRY_CUDA(e, "backward launch");
     return PLSH_OK;
   }
-  PLSH_TRY_CUDA(cudaMallocAsync((void**)&stats, bytes, cs), "backward scratch");
+  plsh::DeviceCtx* ctx = nullptr;
+  if ((st = current_ctx(&ctx)) != PLSH_OK) return st;
+  std::lock_guard<std::mutex> bk(g_bwd_mu);
+  if ((st = scratch_acquire(&ctx->bwd_work, &ctx->bwd_work_bytes, &ctx->bwd_ev, bytes, cs,
+                            "backward scratch")) != PLSH_OK)
+    return st;
+  stats = ctx->bwd_work;
   cudaError_t e = plsh::launch_attn_bwd(Q->data, K->data, V->data, dO->data, dQ->data, dK->data,
                                         dV->data, stats, bins, (int)Q->B, (int)Q->H, (int)K->H,
                                         (int)Q->n, (int)Q->d, causal ? 1 : 0, Q->dtype, cs);
-  const cudaError_t ef = cudaFreeAsync(stats, cs);
-  if (e == cudaSuccess) e = ef;
+  const cudaError_t er = cudaEventRecord(ctx->bwd_ev, cs);
+  if (e == cudaSuccess) e = er;
   PLSH_TRY_CUDA(e, "backward launch");
   return PLSH_OK;
 }
@@ -1078,21 +1111,11 @@ plsh_status plsh_alibi_decode(const plsh_tensor* q, const plsh_tensor* K, const 
   const size_t bytes =
       sizeof(float) * plsh::decode_work_floats((int)q->B, (int)q->H, (int)K->H, (int)q->d,
                                                ctx->num_sms);
-  float* work = nullptr;
-  {
-    std::lock_guard<std::mutex> lk(g_ctx_mu);
-    if (ctx->decode_work_bytes < bytes) {
-      // grow (the old buffer may still be in use by earlier calls)
-      PLSH_TRY_CUDA(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
-      cudaFree(ctx->decode_work);
-      ctx->decode_work = nullptr;
-      ctx->decode_work_bytes = 0;
-      if ((st = dev_alloc((void**)&ctx->decode_work, bytes, "decode partials")) != PLSH_OK)
-        return st;
-      ctx->decode_work_bytes = bytes;
-    }
-    work = ctx->decode_work;
-  }
+  std::lock_guard<std::mutex> dk(g_decode_mu);
+  if ((st = scratch_acquire(&ctx->decode_work, &ctx->decode_work_bytes, &ctx->decode_ev, bytes,
+                            (cudaStream_t)stream, "decode partials")) != PLSH_OK)
+    return st;
+  float* work = ctx->decode_work;
   plsh::DecodeArgs a;
   a.q = q->data;
   a.K = K->data;
@@ -1112,7 +1135,10 @@ plsh_status plsh_alibi_decode(const plsh_tensor* q, const plsh_tensor* K, const 
   a.work = work;
   a.err = ctx->d_err;
   a.wait_ns = ctx->wait_ns;
-  PLSH_TRY_CUDA(plsh::launch_decode(a, (cudaStream_t)stream), "decode launch");
+  cudaError_t e = plsh::launch_decode(a, (cudaStream_t)stream);
+  const cudaError_t er = cudaEventRecord(ctx->decode_ev, (cudaStream_t)stream);
+  if (e == cudaSuccess) e = er;
+  PLSH_TRY_CUDA(e, "decode launch");
   return PLSH_OK;
 }
 

@@ -24,24 +24,38 @@
 //   dV  += P^T dO         (A = P^T from TMEM, B = dO MN-major; cols 256-383)
 //   dK  += dS^T Q         (A = dS^T from TMEM, B = Q MN-major; cols 384-511)
 //   dQ_p = dS K           (A = dS from shared memory, MN-major; B = K MN-major;
-//                          into cols 0-127 once dV has read P^T there)
-// and one thread per key turns a row of S^T, dP^T into P^T, dS^T (bf16): the
-// multiplicity of key j and query i is the number of its bins whose end lies
-// above i (and whose start lies at or below i without the causal mask).  The
-// same threads add each step's dQ_p rows to an fp32 accumulator in global
-// memory (vector atomics; several key tiles reach a query row) and, at the end
-// of an item, write dK and dV of their key.
+//                          into cols 128-255 once dK has read dS^T there)
+// Q is double buffered, so the next step's S^T runs while this step's dQ_p
+// is being drained; the next dP^T waits for that drain.
+//
+// One thread per key turns a row of S^T, dP^T into P^T, dS^T (bf16).  Its
+// multiplicities over a chunk of 32 query rows are a running count: the
+// hashes whose bin around the key is open at the chunk's first row, minus a
+// step at each bin end inside the chunk (plus a step at each bin start when
+// not causal), one bit per row; rows past every bin end or before every start
+// are masked.  Chunks that every bin of every key of the warp spans take
+// c = s, folded into the exponent.  The same threads stage each step's dQ_p
+// rows in shared memory, where TMA reductions add them to an fp32
+// accumulator in global memory (several key tiles reach a query row), and,
+// at the end of an item, write dK and dV of their key.
 //
 // Warps: 0-3 compute (thread = TMEM lane), 4 producer (item queue, query-tile
 // ranges from the bin records, TMA of K, V per item and of Q, dO plus the
-// rows' statistics per step), 5 one thread issuing tcgen05.mma.  Every
-// mbarrier wait is bounded; on expiry the CTA raises the error flag, lets its
-// copies and MMAs drain, frees TMEM and exits.
+// rows' statistics per step, L2 prefetch of the next step's), 5 one thread
+// issuing tcgen05.mma.  Items are taken in the order of their KV group's
+// expected work, largest first.
+// Every mbarrier wait is bounded; on expiry the CTA raises the error flag,
+// lets its copies and MMAs drain, frees TMEM and exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <limits.h>
+#include <math.h>
 #include <stdint.h>
+
+#include <algorithm>
+#include <numeric>
+#include <vector>
 
 #include "bins_dev.cuh"
 #include "plsh_internal.h"
@@ -59,18 +73,20 @@ constexpr int kThreads = 192;
 constexpr int kProdWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kMaxG = 64;                        // query heads per KV head
-constexpr int kMaxSlotsB = 16;                   // bin ends kept per key thread
+constexpr int kMaxSlotsB = 16;                   // bins kept per key thread
+constexpr int kMaxOrder = 64;                    // KV heads with a work order
 constexpr uint32_t kTile = BM * HD * 2;          // 32 KB bf16 tile
 constexpr uint32_t kHalf = kTile / 2;
-constexpr uint32_t OFF_K = 0, OFF_V = kTile, OFF_Q = 2 * kTile, OFF_DO = 3 * kTile,
-                   OFF_DS = 4 * kTile, OFF_END = 5 * kTile;
+constexpr uint32_t OFF_K = 0, OFF_V = kTile, OFF_Q = 2 * kTile,   // two Q buffers
+                   OFF_DO = 4 * kTile, OFF_DS = 5 * kTile, OFF_END = 6 * kTile;
 constexpr uint32_t kTmemCols = 512;
 constexpr unsigned FULL = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
 
 enum {
-  B_KVFULL = 0, B_KVEMPTY, B_QFULL, B_QEMPTY, B_SFULL, B_PDS, B_DQFULL, B_DQEMPTY,
-  B_ACCFULL, B_ACCEMPTY, B_IFULL, B_IFULL1, B_IEMPTY, B_IEMPTY1, B_DRAIN, NUM_BARS
+  B_KVFULL = 0, B_KVEMPTY, B_QFULL, B_QFULL1, B_QEMPTY, B_QEMPTY1, B_DOFULL, B_DOEMPTY,
+  B_SFULL, B_PDS, B_DQFULL, B_DQEMPTY, B_ACCFULL, B_ACCEMPTY, B_IFULL, B_IFULL1, B_IEMPTY,
+  B_IEMPTY1, B_DRAIN, NUM_BARS
 };
 
 struct ItemB {
@@ -81,7 +97,11 @@ struct ItemB {
 struct CtlB {
   uint64_t bars[NUM_BARS];
   ItemB ring[2];
-  float stats[2][BQ][3];                         // m, 1/l, Delta of the step's rows
+  // per step buffer: -(m + log2 l) of the step's rows, then their Delta
+  alignas(16) float stats[2][2][BQ];
+  // per step buffer: the bin records of the step's head over the item's four
+  // 32-key words, per hash
+  uint4 recs[2][kMaxSlotsB][BM / 32];
   uint32_t tmem_base;
   int abort;
 };
@@ -90,12 +110,14 @@ struct BwdTcParams {
   const BinRecord* rec;
   int s;
   int64_t W;
-  int B, Hq, Hkv, n, causal;
+  int B, Hq, Hkv, n;
   const float* stats;                            // [B * Hq * n][3]
   float* dq_acc;                                 // [B * Hq * n][128] fp32, zeroed
   __nv_bfloat16* dK;                             // [B, Hkv, n, 128]
   __nv_bfloat16* dV;
   int num_items;                                 // B * Hkv * key tiles
+  int ordered;                                   // kv_order holds the KV heads' order
+  int kv_order[kMaxOrder];
   int* queue;                                    // {next item, finished CTAs}
   int* err;
   uint64_t wait_ns;
@@ -126,10 +148,100 @@ __device__ __forceinline__ void step_of(const CtlB* ctl, int slot, int G, int k,
   qt = 0;
 }
 
+// TMA reduction of a shared-memory box into global memory (add), tracked by
+// the issuing thread's bulk async-group.
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, uint32_t src, int x,
+                                                  int y, int z) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], "
+      "[%1];" ::"l"(map), "r"(src), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// the group's reads of shared memory are done (the writes may still be in flight)
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// A box of a tensor into L2 ahead of its load.
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
+// Rows [a, b] of a 32-row chunk as a bit mask (relative to the chunk).
+__device__ __forceinline__ uint32_t row_mask(int a, int b) {
+  if (a > 31 || b < 0 || a > b) return 0u;
+  const uint32_t up = b >= 31 ? 0xffffffffu : ((2u << b) - 1u);
+  const uint32_t dn = a <= 0 ? 0xffffffffu : ~((1u << a) - 1u);
+  return up & dn;
+}
+
+// Adds one step at the positions of `m` to a five-plane binary counter.
+__device__ __forceinline__ void plane_add5(uint32_t (&pl)[5], uint32_t m) {
+#pragma unroll
+  for (int b = 0; b < 5; ++b) {
+    const uint32_t c = pl[b] & m;
+    pl[b] ^= m;
+    m = c;
+  }
+}
+
+// Multiplies the chunk's weights by the running count c(e): base plus the
+// steps at rows 1..e, up steps (bin starts, non-causal only) adding and dn
+// steps (bin ends) subtracting; one bit per step, four independent runs of
+// eight rows.
+template <bool UP>
+__device__ __forceinline__ void count_steps(float (&pv)[32], int base, uint32_t up, uint32_t dn) {
+  float c[4];
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    const uint32_t le = (2u << (8 * g)) - 1u;    // rows 0 .. 8g
+    int cb = base - __popc(dn & le);
+    if (UP) cb += __popc(up & le);
+    c[g] = (float)cb;
+  }
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const int e = 8 * g + k;
+      if (k > 0) {
+        if (dn & (1u << e)) c[g] -= 1.f;
+        if (UP && (up & (1u << e))) c[g] += 1.f;
+      }
+      pv[e] *= c[g];
+    }
+  }
+}
+
+// The same with several steps at one row: binary planes of the step counts.
+template <bool UP>
+__device__ __forceinline__ void count_planes(float (&pv)[32], int base, const uint32_t (&up)[5],
+                                             const uint32_t (&dn)[5]) {
+#pragma unroll
+  for (int e = 0; e < 32; ++e) {
+    const uint32_t le = e == 31 ? 0xffffffffu : ((2u << e) - 1u);
+    int cb = base;
+#pragma unroll
+    for (int b = 0; b < 5; ++b) {
+      cb -= __popc(dn[b] & le) << b;
+      if (UP) cb += __popc(up[b] & le) << b;
+    }
+    pv[e] *= (float)cb;
+  }
+}
+
+template <bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-              const __grid_constant__ BwdTcParams p) {
+              const __grid_constant__ CUtensorMap tmAcc, const __grid_constant__ BwdTcParams p) {
   extern __shared__ uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -146,8 +258,12 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   if (threadIdx.x == 0) {
     mbar_init(bar(B_KVFULL), 1);
     mbar_init(bar(B_KVEMPTY), 1);
-    mbar_init(bar(B_QFULL), 1);
-    mbar_init(bar(B_QEMPTY), 1);
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(bar(B_QFULL + k), 1);
+      mbar_init(bar(B_QEMPTY + k), 4);           // the compute warps, once dQ staged there is read
+    }
+    mbar_init(bar(B_DOFULL), 1);
+    mbar_init(bar(B_DOEMPTY), 1);
     mbar_init(bar(B_SFULL), 1);
     mbar_init(bar(B_PDS), BM);
     mbar_init(bar(B_DQFULL), 1);
@@ -171,6 +287,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     prefetch_tensormap(&tmK);
     prefetch_tensormap(&tmV);
     prefetch_tensormap(&tmDO);
+    prefetch_tensormap(&tmAcc);
   }
   tc_fence_before();
   __syncthreads();
@@ -182,6 +299,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     // ------------------------------------------------ producer / scheduler
     bool ok = true;
     int gstep = 0;                               // steps loaded so far (all items)
+    int nq0 = 0, nq1 = 0;                        // Q loads per buffer
+    int ndo = 0;                                 // dO loads
     int kv_loads = 0;                            // items whose K and V were loaded
     for (int seq = 0; ok; ++seq) {
       const int slot = seq & 1;
@@ -194,7 +313,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       ok = __shfl_sync(FULL, (int)ok, 0) != 0;
       idx = __shfl_sync(FULL, idx, 0);
       if (!ok) break;
-      volatile int* it = reinterpret_cast<volatile int*>(&ctl->ring[slot]);
+      ItemB* ring = &ctl->ring[slot];
+      volatile int* it = reinterpret_cast<volatile int*>(ring);
       if (idx >= p.num_items) {
         if (lane == 0) {
           it[0] = 0;
@@ -202,33 +322,56 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         }
         break;
       }
-      // key tiles in ascending order (the first ones reach the most rows)
-      const int kt = idx % KT, bk = idx / KT;
-      const int kvh = bk % p.Hkv, b = bk / p.Hkv;
+      // KV groups in the host's order, then batch elements, then key tiles
+      // in ascending order (the first ones reach the most rows)
+      const int per = p.B * KT;
+      const int gs = idx / per, rem = idx - (idx / per) * per;
+      const int b = rem / KT, kt = rem - (rem / KT) * KT;
+      const int kvh = p.ordered ? p.kv_order[gs] : gs;
       const int j_first = kt * BM, j_last = min(kt * BM + BM - 1, n - 1);
-      // query tiles whose rows share a bin with a key of this tile, per head
-      int steps = 0;
-      for (int hg = 0; hg < G; ++hg) {
-        const int h = kvh * G + hg;
-        int hmax = j_last + 1, lmin = j_first;
-        for (int t = lane; t < s; t += 32) {
-          const BinRecord rl = load_record(p.rec, ((int64_t)h * s + t) * p.W + (j_last >> 5));
-          hmax = max(hmax, bin_hi(rl, j_last));
-          if (!p.causal) {
-            const BinRecord rf = load_record(p.rec, ((int64_t)h * s + t) * p.W + (j_first >> 5));
-            lmin = min(lmin, bin_lo(rf, j_first));
+      // query tiles whose rows share a bin with a key of this tile, per
+      // head: the (head, hash) records spread over the lanes and combined in
+      // shared memory
+      for (int hg = lane; hg < G; hg += 32) {
+        ring->hi[hg] = j_last + 1;
+        ring->lo[hg] = j_first;
+      }
+      __syncwarp();
+      const int GS = G * s;
+      for (int base = 0; base < GS; base += 128) {
+        BinRecord rl[4], rf[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int ht = base + u * 32 + lane;
+          if (ht < GS) {
+            const int hg = ht / s, t = ht - (ht / s) * s;
+            const int64_t rb = ((int64_t)(kvh * G + hg) * s + t) * p.W;
+            rl[u] = load_record(p.rec, rb + (j_last >> 5));
+            if (!CAUSAL) rf[u] = load_record(p.rec, rb + (j_first >> 5));
           }
         }
-        hmax = __reduce_max_sync(FULL, hmax);
-        lmin = __reduce_min_sync(FULL, lmin);
-        const int qlo = p.causal ? kt : lmin / BQ;
-        const int qhi = (hmax + BQ - 1) / BQ;
-        if (lane == 0) {
-          it[5 + hg] = qlo;                      // ring[slot].lo[hg]
-          it[5 + kMaxG + hg] = qhi;              // ring[slot].hi[hg]
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int ht = base + u * 32 + lane;
+          if (ht < GS) {
+            const int hg = ht / s;
+            atomicMax(&ring->hi[hg], bin_hi(rl[u], j_last));
+            if (!CAUSAL) atomicMin(&ring->lo[hg], bin_lo(rf[u], j_first));
+          }
         }
+      }
+      __syncwarp();
+      int steps = 0;
+      for (int hg = lane; hg < G; hg += 32) {
+        const int qlo = CAUSAL ? kt : ring->lo[hg] / BQ;
+        const int qhi = (ring->hi[hg] + BQ - 1) / BQ;
+        ring->lo[hg] = qlo;
+        ring->hi[hg] = qhi;
         steps += qhi - qlo;
       }
+      steps = __reduce_add_sync(FULL, steps);
+      __threadfence_block();
+      __syncwarp();
       if (lane == 0) {
         it[0] = 1;
         it[1] = b;
@@ -252,39 +395,89 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         }
       }
       ok = __shfl_sync(FULL, (int)ok, 0) != 0;
-      // per step: the rows' statistics, then Q and dO
+      // the rows' statistics of the next step, read ahead into registers
+      float sm[4], sl[4], sd[4];
+      uint4 rr[2];
+      auto load_stats = [&](int k) {
+        int hg, qt;
+        step_of(ctl, slot, G, k, hg, qt);
+        const int64_t rowbase = ((int64_t)b * p.Hq + kvh * G + hg) * n;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int tw = u * 32 + lane;          // (hash, word of the key tile)
+          rr[u] = make_uint4(0u, 0u, 0u, 0u);
+          if (tw < s * 4) {
+            const int64_t word = min((int64_t)kt * 4 + (tw & 3), p.W - 1);
+            rr[u] = __ldg(reinterpret_cast<const uint4*>(p.rec) +
+                          ((int64_t)(kvh * G + hg) * s + (tw >> 2)) * p.W + word);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = qt * BQ + u * 32 + lane;
+          sm[u] = 0.f;
+          sl[u] = 0.f;
+          sd[u] = 0.f;
+          if (i < n) {
+            const float* st = p.stats + (rowbase + i) * 3;
+            sm[u] = __ldg(st);
+            sl[u] = __ldg(st + 1);
+            sd[u] = __ldg(st + 2);
+          }
+        }
+      };
+      if (ok && steps > 0) load_stats(0);
       for (int k = 0; ok && k < steps; ++k, ++gstep) {
         int hg, qt;
         step_of(ctl, slot, G, k, hg, qt);
-        const int h = kvh * G + hg;
-        if (lane == 0) ok = mbar_wait(bar(B_QEMPTY), ((uint32_t)gstep & 1u) ^ 1u, abort, lim);
+        const int plane = b * p.Hq + kvh * G + hg;
+        const int qb = gstep & 1;
+        // Q into its buffer once the step two back has finished dK
+        if (lane == 0) {
+          ok = mbar_wait(bar(B_QEMPTY + qb), ((uint32_t)(gstep >> 1) & 1u) ^ 1u, abort, lim);
+          if (ok) {
+            const uint32_t dst = sbase + OFF_Q + (uint32_t)qb * kTile;
+            mbar_arrive_expect_tx(bar(B_QFULL + qb), kTile);
+            tma_load_3d(dst, &tmQ, bar(B_QFULL + qb), 0, qt * BQ, plane);
+            tma_load_3d(dst + kHalf, &tmQ, bar(B_QFULL + qb), 64, qt * BQ, plane);
+            if (qb) ++nq1;
+            else ++nq0;
+          }
+        }
         ok = __shfl_sync(FULL, (int)ok, 0) != 0;
         if (!ok) break;
-        const int buf = gstep & 1;
-        const int64_t rowbase = ((int64_t)b * p.Hq + h) * n;
-        for (int r = lane; r < BQ; r += 32) {
-          const int i = qt * BQ + r;
-          float m = 0.f, il = 0.f, dl = 0.f;
-          if (i < n) {
-            const float* st = p.stats + (rowbase + i) * 3;
-            m = st[0];
-            il = st[1] > 0.f ? 1.f / st[1] : 0.f;
-            dl = st[2];
-          }
-          ctl->stats[buf][r][0] = m;
-          ctl->stats[buf][r][1] = il;
-          ctl->stats[buf][r][2] = dl;
+        // dO and the rows' statistics once the step before has finished dV
+        if (lane == 0) ok = mbar_wait(bar(B_DOEMPTY), ((uint32_t)gstep & 1u) ^ 1u, abort, lim);
+        ok = __shfl_sync(FULL, (int)ok, 0) != 0;
+        if (!ok) break;
+        float* sv = ctl->stats[gstep & 1][0];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int r = u * 32 + lane;
+          sv[r] = sl[u] > 0.f ? -(sm[u] + lg2(sl[u])) : -INFINITY;
+          sv[BQ + r] = sd[u];
         }
+        uint4* rv = &ctl->recs[gstep & 1][0][0];
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+          if (u * 32 + lane < s * 4) rv[u * 32 + lane] = rr[u];
         __syncwarp();
         if (lane == 0) {
-          const int plane = b * p.Hq + h;
-          mbar_arrive_expect_tx(bar(B_QFULL), 2 * kTile);
-          tma_load_3d(sbase + OFF_Q, &tmQ, bar(B_QFULL), 0, qt * BQ, plane);
-          tma_load_3d(sbase + OFF_Q + kHalf, &tmQ, bar(B_QFULL), 64, qt * BQ, plane);
-          tma_load_3d(sbase + OFF_DO, &tmDO, bar(B_QFULL), 0, qt * BQ, plane);
-          tma_load_3d(sbase + OFF_DO + kHalf, &tmDO, bar(B_QFULL), 64, qt * BQ, plane);
+          mbar_arrive_expect_tx(bar(B_DOFULL), kTile);
+          tma_load_3d(sbase + OFF_DO, &tmDO, bar(B_DOFULL), 0, qt * BQ, plane);
+          tma_load_3d(sbase + OFF_DO + kHalf, &tmDO, bar(B_DOFULL), 64, qt * BQ, plane);
+          ++ndo;
         }
         __syncwarp();
+        if (k + 1 < steps) {
+          load_stats(k + 1);
+          // the next step's Q and dO into L2 while this step runs
+          int hg2, qt2;
+          step_of(ctl, slot, G, k + 1, hg2, qt2);
+          const int plane2 = b * p.Hq + kvh * G + hg2;
+          if (lane < 4)
+            tma_prefetch_3d(lane < 2 ? &tmQ : &tmDO, (lane & 1) * 64, qt2 * BQ, plane2);
+        }
       }
     }
     if (!ok && lane == 0) {
@@ -292,9 +485,12 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       atomicOr(p.err, 1);
     }
     // every copy this warp started lands before the CTA can exit
-    if (lane == 0 && gstep > 0) mbar_wait(bar(B_QFULL), (uint32_t)(gstep - 1) & 1u, nullptr, lim);
-    if (lane == 0 && kv_loads > 0)
-      mbar_wait(bar(B_KVFULL), (uint32_t)(kv_loads - 1) & 1u, nullptr, lim);
+    if (lane == 0) {
+      if (nq0 > 0) mbar_wait(bar(B_QFULL), (uint32_t)(nq0 - 1) & 1u, nullptr, lim);
+      if (nq1 > 0) mbar_wait(bar(B_QFULL1), (uint32_t)(nq1 - 1) & 1u, nullptr, lim);
+      if (ndo > 0) mbar_wait(bar(B_DOFULL), (uint32_t)(ndo - 1) & 1u, nullptr, lim);
+      if (kv_loads > 0) mbar_wait(bar(B_KVFULL), (uint32_t)(kv_loads - 1) & 1u, nullptr, lim);
+    }
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ----------------------------------------------------------- MMA issue
@@ -304,10 +500,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       constexpr uint32_t id_mm = idesc_bf16_f32(BQ, HD, 1, 1);   // dQ_p (both MN-major)
       const uint64_t dK0 = desc_sw128(sbase + OFF_K, 16, 1024);
       const uint64_t dV0 = desc_sw128(sbase + OFF_V, 16, 1024);
-      const uint64_t dQ0 = desc_sw128(sbase + OFF_Q, 16, 1024);
       const uint64_t dO0 = desc_sw128(sbase + OFF_DO, 16, 1024);
       const uint64_t dOm = desc_sw128(sbase + OFF_DO, kHalf, 1024);   // dO, MN-major
-      const uint64_t dQm = desc_sw128(sbase + OFF_Q, kHalf, 1024);    // Q, MN-major
       const uint64_t dKm = desc_sw128(sbase + OFF_K, kHalf, 1024);    // K, MN-major
       const uint64_t dSm = desc_sw128(sbase + OFF_DS, kHalf, 1024);   // dS, MN-major
       bool ok = true;
@@ -320,20 +514,29 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         read_itemb(ctl, slot, it);
         if (!it.valid) break;
         ok = mbar_wait(bar(B_KVFULL), (uint32_t)seq & 1u, abort, lim);
-        // the compute threads have read the item before's dV, dK
-        if (ok && seq > 0) ok = mbar_wait(bar(B_ACCEMPTY), (uint32_t)(seq - 1) & 1u, abort, lim);
         for (int k = 0; ok && k < it.steps; ++k, ++gstep) {
-          ok = mbar_wait(bar(B_QFULL), (uint32_t)gstep & 1u, abort, lim);
-          if (ok && gstep > 0)
-            ok = mbar_wait(bar(B_DQEMPTY), (uint32_t)(gstep - 1) & 1u, abort, lim);
+          const int qb = gstep & 1;
+          const uint32_t q_addr = sbase + OFF_Q + (uint32_t)qb * kTile;
+          const uint64_t dQ0 = desc_sw128(q_addr, 16, 1024);
+          const uint64_t dQm = desc_sw128(q_addr, kHalf, 1024);       // Q, MN-major
+          ok = mbar_wait(bar(B_QFULL + qb), (uint32_t)(gstep >> 1) & 1u, abort, lim);
           if (!ok) break;
           tc_fence_after();
-          // S^T = K Q^T and dP^T = V dO^T over the head dimension
+          // S^T = K Q^T over the head dimension (the products before have
+          // read P^T from these columns: tcgen05 MMAs of one thread run in
+          // issue order)
 #pragma unroll
           for (int kk = 0; kk < HD / 16; ++kk) {
             const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
             mma_bf16_ss(tmem, desc_add(dK0, off), desc_add(dQ0, off), id_kk, kk > 0 ? 1u : 0u);
           }
+          // dP^T = V dO^T, once dO has landed and the step before's dQ_p
+          // has been read out of columns 128-255
+          ok = mbar_wait(bar(B_DOFULL), (uint32_t)gstep & 1u, abort, lim);
+          if (ok && gstep > 0)
+            ok = mbar_wait(bar(B_DQEMPTY), (uint32_t)(gstep - 1) & 1u, abort, lim);
+          if (!ok) break;
+          tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < HD / 16; ++kk) {
             const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
@@ -341,7 +544,10 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                         kk > 0 ? 1u : 0u);
           }
           mma_commit(bar(B_SFULL));
-          ok = mbar_wait(bar(B_PDS), (uint32_t)gstep & 1u, abort, lim);
+          // the compute threads have read the item before's dV, dK
+          if (k == 0 && seq > 0)
+            ok = mbar_wait(bar(B_ACCEMPTY), (uint32_t)(seq - 1) & 1u, abort, lim);
+          if (ok) ok = mbar_wait(bar(B_PDS), (uint32_t)gstep & 1u, abort, lim);
           if (!ok) break;
           tc_fence_after();
           // dV += P^T dO and dK += dS^T Q over the step's queries; P^T and
@@ -352,22 +558,24 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             mma_f16kind_ts(tmem + 256, tmem + ac, desc_add(dOm, kk * (2048 >> 4)), id_tm,
                            (k == 0 && kk == 0) ? 0u : 1u);
           }
+          mma_commit(bar(B_DOEMPTY));
 #pragma unroll
           for (int kk = 0; kk < BQ / 16; ++kk) {
             const uint32_t ac = 128 + (kk >> 1) * 32 + (kk & 1) * 8;
             mma_f16kind_ts(tmem + 384, tmem + ac, desc_add(dQm, kk * (2048 >> 4)), id_tm,
                            (k == 0 && kk == 0) ? 0u : 1u);
           }
-          mma_commit(bar(B_QEMPTY));
-          // dQ_p = dS K over the tile's keys, into columns 0-127 (the
-          // products above have read P^T from there: tcgen05 MMAs of one
-          // thread run in issue order)
+          // dQ_p = dS K over the tile's keys, into columns 128-255
 #pragma unroll
           for (int kk = 0; kk < BM / 16; ++kk)
-            mma_bf16_ss(tmem, desc_add(dSm, kk * (2048 >> 4)), desc_add(dKm, kk * (2048 >> 4)),
-                        id_mm, kk > 0 ? 1u : 0u);
+            mma_bf16_ss(tmem + 128, desc_add(dSm, kk * (2048 >> 4)),
+                        desc_add(dKm, kk * (2048 >> 4)), id_mm, kk > 0 ? 1u : 0u);
           mma_commit(bar(B_DQFULL));
         }
+        if (!ok) break;
+        // an item without steps still hands its (zero) gradients over in turn
+        if (it.steps == 0 && seq > 0)
+          ok = mbar_wait(bar(B_ACCEMPTY), (uint32_t)(seq - 1) & 1u, abort, lim);
         if (!ok) break;
         // dV, dK complete; K and V free
         mma_commit(bar(B_ACCFULL));
@@ -388,7 +596,12 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t t_s = tmem + lane_base, t_dp = t_s + 128, t_dv = t_s + 256, t_dk = t_s + 384;
     const float scale_log2 = kLog2e * 0.08838834764831845f;      // log2(e) / sqrt(128)
+    const uint64_t scale2 = f2_pack(scale_log2, scale_log2);
     const uint32_t ds_row = sbase + OFF_DS + (uint32_t)r * 128u;  // this key's row of dS^T
+    const int wq = warp & 3;
+    // the warp's rows of the two dS^T halves, 4 KB each (1024-byte aligned)
+    const uint32_t wpiece0 = sbase + OFF_DS + (uint32_t)wq * 4096u;
+    const uint32_t wpiece1 = wpiece0 + kHalf;
     bool ok = true;
     int gstep = 0;
     for (int seq = 0; ok; ++seq) {
@@ -402,65 +615,169 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       const bool key_ok = j < n;
       const int jj = min(j, n - 1);
       int cur_h = -1;
+      // this key's bins under the head's hashes, [lo_t, hi_t), and the rows
+      // [ilo, ihi] that share at least one of them
       int his[kMaxSlotsB], los[kMaxSlotsB];
+      int ilo = 0, ihi = -1, himin = 0, lomax = 0;
       for (int k = 0; ok && k < it.steps; ++k, ++gstep) {
         int hg, qt;
         step_of(ctl, slot, G, k, hg, qt);
         const int h = it.kvh * G + hg;
+        const float* sv = ctl->stats[gstep & 1][0];
+        // the step's row statistics and bin records have landed
+        ok = __all_sync(FULL, mbar_wait(bar(B_DOFULL), (uint32_t)gstep & 1u, abort, lim));
+        if (!ok) break;
         if (h != cur_h) {
-          // this key's bins under the head's hashes: [lo_t, hi_t)
+          const uint4* rv = &ctl->recs[gstep & 1][0][(jj >> 5) - it.kt * (BM / 32)];
+          int hmax = 0, lmin = INT_MAX;
+          himin = INT_MAX;
+          lomax = 0;
 #pragma unroll
           for (int t = 0; t < kMaxSlotsB; ++t) {
-            his[t] = INT_MIN;
-            los[t] = INT_MAX;
+            his[t] = CAUSAL ? -1 : (1 << 30);    // unused slots: no count, no step
+            los[t] = 1 << 30;
             if (t < s) {
-              const BinRecord rc = load_record(p.rec, ((int64_t)h * s + t) * p.W + (jj >> 5));
+              const uint4 v = rv[t * (BM / 32)];
+              BinRecord rc;
+              rc.bits = v.x;
+              rc.prev = (int32_t)v.y;
+              rc.next = (int32_t)v.z;
+              rc.pad = 0;
               his[t] = bin_hi(rc, jj);
               los[t] = bin_lo(rc, jj);
+              hmax = max(hmax, his[t]);
+              himin = min(himin, his[t]);
+              lmin = min(lmin, los[t]);
+              lomax = max(lomax, los[t]);
             }
           }
+          ilo = CAUSAL ? j : lmin;
+          ihi = key_ok ? min(hmax, n) - 1 : -1;
           cur_h = h;
         }
-        const int buf = gstep & 1;
-        ok = __all_sync(FULL, mbar_wait(bar(B_QFULL), (uint32_t)gstep & 1u, abort, lim) &&
-                                  mbar_wait(bar(B_SFULL), (uint32_t)gstep & 1u, abort, lim));
+        ok = __all_sync(FULL, mbar_wait(bar(B_SFULL), (uint32_t)gstep & 1u, abort, lim));
         if (!ok) break;
         tc_fence_after();
+        // the copy engine has read the step before's staged dQ rows: the
+        // warp's dS^T rows may be written again and that step's Q buffer is
+        // free for the producer
+        if (lane == 0) {
+          bulk_wait_read();
+          if (gstep > 0) mbar_arrive(bar(B_QEMPTY + ((gstep - 1) & 1)));
+        }
+        __syncwarp();
         const int i0 = qt * BQ;
 #pragma unroll 1
         for (int q = 0; q < 4; ++q) {
-          uint32_t sv[32], dv[32];
-          tmem_ld32(t_s + q * 32, sv);
-          tmem_ld32(t_dp + q * 32, dv);
+          const int ic = i0 + q * 32;
+          const uint32_t vm = row_mask(ilo - ic, ihi - ic);
+          const uint32_t half = (uint32_t)(q >> 1);
+          if (!__any_sync(FULL, vm != 0u)) {
+            // no row of the chunk shares a bin with a key of this warp
+            const uint32_t z[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u,
+                                    0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+            tmem_st16(t_s + q * 32, z);
+            tmem_st16(t_dp + q * 32, z);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const uint32_t c16 = (uint32_t)((q & 1) * 4 + v);
+              st_shared_v4(ds_row + half * kHalf + ((c16 ^ (uint32_t)(r & 7)) << 4), 0u, 0u, 0u,
+                           0u);
+            }
+            continue;
+          }
+          uint32_t sv32[32], dv32[32];
+          tmem_ld32(t_s + q * 32, sv32);
+          tmem_ld32(t_dp + q * 32, dv32);
+          // multiplicities over the chunk's rows: base at its first row,
+          // steps inside it
+          int base = s;
+          bool flat = true, multi = false;
+          uint32_t up[5] = {0u, 0u, 0u, 0u, 0u}, dn[5] = {0u, 0u, 0u, 0u, 0u};
+          const bool deep = himin > ic + 31 && (CAUSAL || lomax <= ic);
+          if (!__all_sync(FULL, deep || vm == 0u)) {
+            int ch = 0, cl = 0;
+            uint32_t u0 = 0u, d0 = 0u, x0 = 0u;
+#pragma unroll
+            for (int t = 0; t < kMaxSlotsB; ++t) {
+              if (t >= s) break;
+              const int dh = his[t] - ic;
+              ch += dh > 0 ? 1 : 0;
+              const uint32_t bh = shl_clamp(2u, dh - 1);
+              x0 |= d0 & bh;
+              d0 |= bh;
+              if (!CAUSAL) {
+                const int dl = los[t] - ic;
+                cl += dl > 0 ? 0 : 1;
+                const uint32_t bl = shl_clamp(2u, dl - 1);
+                x0 |= u0 & bl;
+                u0 |= bl;
+              }
+            }
+            base = CAUSAL ? ch : ch + cl - s;
+            if (vm == 0u) {
+              u0 = 0u;
+              d0 = 0u;
+              x0 = 0u;
+            }
+            up[0] = u0;
+            dn[0] = d0;
+            flat = (u0 | d0) == 0u;
+            multi = __any_sync(FULL, x0 != 0u);
+            if (multi) {
+              // several bin ends (or starts) at one row
+              up[0] = 0u;
+              dn[0] = 0u;
+              if (vm != 0u) {
+#pragma unroll
+                for (int t = 0; t < kMaxSlotsB; ++t) {
+                  if (t >= s) break;
+                  plane_add5(dn, shl_clamp(2u, his[t] - ic - 1));
+                  if (!CAUSAL) plane_add5(up, shl_clamp(2u, los[t] - ic - 1));
+                }
+              }
+            }
+          }
+          const bool all_flat = __all_sync(FULL, flat);
+          const float lgb = all_flat ? lg2((float)max(base, 1)) : 0.f;
+          const uint64_t lgb2 = f2_pack(lgb, lgb);
           tmem_wait_ld();
+          float pv[32];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float2 nm = *reinterpret_cast<const float2*>(sv + q * 32 + e);
+            const uint64_t a2 =
+                f2_fma(f2_pack(__uint_as_float(sv32[e]), __uint_as_float(sv32[e + 1])), scale2,
+                       f2_add(f2_pack(nm.x, nm.y), lgb2));
+            f2_unpack(a2, pv[e], pv[e + 1]);
+          }
+          if (__any_sync(FULL, vm != 0xffffffffu)) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (!(vm & (1u << e))) pv[e] = -INFINITY;
+          }
+#pragma unroll
+          for (int e = 0; e < 32; ++e) pv[e] = ex2(pv[e]);
+          if (!all_flat) {
+            if (multi) count_planes<!CAUSAL>(pv, base, up, dn);
+            else count_steps<!CAUSAL>(pv, base, up[0], dn[0]);
+          }
           uint32_t pk[16], dk[16];
 #pragma unroll
-          for (int e2 = 0; e2 < 16; ++e2) {
-            float pe[2], de[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int e = 2 * e2 + u;
-              const int i = i0 + q * 32 + e;
-              int c = 0;
-#pragma unroll
-              for (int t = 0; t < kMaxSlotsB; ++t)
-                c += (his[t] > i && los[t] <= i) ? 1 : 0;
-              const bool live = key_ok && i < n && c > 0 && (!p.causal || i >= j);
-              const float* st = ctl->stats[buf][q * 32 + e];
-              const float pv = live ? (float)c * ex2(fmaf(__uint_as_float(sv[e]), scale_log2,
-                                                          -st[0])) * st[1]
-                                    : 0.f;
-              pe[u] = pv;
-              de[u] = pv * (__uint_as_float(dv[e]) - st[2]);
-            }
-            pk[e2] = pack_bf16(pe[0], pe[1]);
-            dk[e2] = pack_bf16(de[0], de[1]);
+          for (int e = 0; e < 32; e += 2) {
+            const float2 dl = *reinterpret_cast<const float2*>(sv + BQ + q * 32 + e);
+            const uint64_t g2 =
+                f2_sub(f2_pack(__uint_as_float(dv32[e]), __uint_as_float(dv32[e + 1])),
+                       f2_pack(dl.x, dl.y));
+            float d0, d1;
+            f2_unpack(f2_mul(f2_pack(pv[e], pv[e + 1]), g2), d0, d1);
+            pk[e >> 1] = pack_bf16(pv[e], pv[e + 1]);
+            dk[e >> 1] = pack_bf16(d0, d1);
           }
           tmem_st16(t_s + q * 32, pk);
           tmem_st16(t_dp + q * 32, dk);
           // dS^T into shared memory as the MN-major A operand of dQ_p: two
           // 64-query halves of 128 key rows x 128 bytes, 128-byte swizzle
-          const uint32_t half = (uint32_t)(q >> 1);
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             const uint32_t c16 = (uint32_t)((q & 1) * 4 + v);
@@ -472,25 +789,46 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(bar(B_PDS));
-        // this step's dQ rows (TMEM lane = query row) into the accumulator
+        // this step's dQ rows (TMEM lane = query row) into the accumulator:
+        // each warp stages its 32 rows as four 128-byte swizzled fp32 boxes
+        // of 32 columns in the 4 KB pieces that hold its own rows of the dS
+        // buffer and of the step's Q buffer (both free once dQ_p has run),
+        // which TMA adds to the accumulator; the warp waits for the copy
+        // engine's reads only before it next writes there (the start of the
+        // next step, which also hands the Q buffer back)
         ok = __all_sync(FULL, mbar_wait(bar(B_DQFULL), (uint32_t)gstep & 1u, abort, lim));
         if (!ok) break;
         tc_fence_after();
         {
-          const int i = i0 + r;
-          float4* dst = reinterpret_cast<float4*>(p.dq_acc + (((int64_t)it.b * p.Hq + h) * n + i) * HD);
+          const int row0 = i0 + wq * 32;
+          const int plane = it.b * p.Hq + h;
+          const uint32_t qpiece = sbase + OFF_Q + (uint32_t)(gstep & 1) * kTile + (uint32_t)wq * 4096u;
 #pragma unroll 1
-          for (int q = 0; q < 4; ++q) {
-            uint32_t o[32];
-            tmem_ld32(t_s + q * 32, o);
+          for (int bx = 0; bx < 4; bx += 2) {
+            uint32_t o[64];
+            tmem_ld32(t_dp + bx * 32, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
+            tmem_ld32(t_dp + bx * 32 + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
             tmem_wait_ld();
-            if (i < n) {
 #pragma unroll
-              for (int v = 0; v < 8; ++v)
-                atomicAdd(dst + q * 8 + v,
-                          make_float4(__uint_as_float(o[4 * v]), __uint_as_float(o[4 * v + 1]),
-                                      __uint_as_float(o[4 * v + 2]), __uint_as_float(o[4 * v + 3])));
+            for (int u = 0; u < 2; ++u) {
+              const int box = bx + u;
+              const uint32_t base = box == 0 ? wpiece0 : box == 1 ? wpiece1 : box == 2 ? qpiece
+                                                                                       : qpiece + kHalf;
+              const uint32_t row = base + (uint32_t)lane * 128u;
+#pragma unroll
+              for (int c = 0; c < 8; ++c)
+                st_shared_v4(row + (((uint32_t)c ^ (uint32_t)(lane & 7)) << 4), o[32 * u + 4 * c],
+                             o[32 * u + 4 * c + 1], o[32 * u + 4 * c + 2], o[32 * u + 4 * c + 3]);
             }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && row0 < n) {
+            tma_reduce_add_3d(&tmAcc, wpiece0, 0, row0, plane);
+            tma_reduce_add_3d(&tmAcc, wpiece1, 32, row0, plane);
+            tma_reduce_add_3d(&tmAcc, qpiece, 64, row0, plane);
+            tma_reduce_add_3d(&tmAcc, qpiece + kHalf, 96, row0, plane);
+            bulk_commit();
           }
         }
         tc_fence_before();
@@ -544,6 +882,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     }
   }
 
+  // the accumulator's reductions are complete before the CTA exits
+  if (warp < 4 && lane == 0) bulk_wait_all();
   tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {
@@ -570,6 +910,33 @@ __global__ void dq_convert_kernel(const float4* __restrict__ acc, uint2* __restr
   out[i] = make_uint2(pack_bf16(v.x * inv, v.y * inv), pack_bf16(v.z * inv, v.w * inv));
 }
 
+typedef CUresult (*EncodeTiledFnB)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The dQ accumulator [planes, n, 128] fp32 as a 3-D tensor with 32 x 32 x 1
+// boxes (128-byte rows) and 128-byte swizzle; rows past n are not written.
+bool make_acc_map(CUtensorMap* map, float* base, int64_t planes, int64_t n) {
+  static EncodeTiledFnB fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return false;
+    fn = reinterpret_cast<EncodeTiledFnB>(ptr);
+  }
+  const cuuint64_t dims[3] = {(cuuint64_t)HD, (cuuint64_t)n, (cuuint64_t)planes};
+  const cuuint64_t strides[2] = {(cuuint64_t)HD * 4, (cuuint64_t)n * HD * 4};
+  const cuuint32_t box[3] = {32, 32, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 size_t bwd_tc_smem_bytes() { return 1024 + OFF_END + sizeof(CtlB); }
@@ -579,11 +946,12 @@ cudaError_t launch_attn_bwd_tc(const void* Q, const void* K, const void* V, cons
                                const plsh_bins* bn, int B, int Hq, int Hkv, int n, int causal,
                                int* queue, int* err, uint64_t wait_ns, int num_sms,
                                cudaStream_t st) {
-  CUtensorMap mq, mk, mv, mdo;
+  CUtensorMap mq, mk, mv, mdo, macc;
   if (!make_tile_map_bf16(&mq, Q, (int64_t)B * Hq, n) ||
       !make_tile_map_bf16(&mk, K, (int64_t)B * Hkv, n) ||
       !make_tile_map_bf16(&mv, V, (int64_t)B * Hkv, n) ||
-      !make_tile_map_bf16(&mdo, dO, (int64_t)B * Hq, n))
+      !make_tile_map_bf16(&mdo, dO, (int64_t)B * Hq, n) ||
+      !make_acc_map(&macc, dq_acc, (int64_t)B * Hq, n))
     return cudaErrorInvalidValue;
   BwdTcParams p;
   p.rec = bn->d_rec;
@@ -593,22 +961,37 @@ cudaError_t launch_attn_bwd_tc(const void* Q, const void* K, const void* V, cons
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.n = n;
-  p.causal = causal;
   p.stats = stats;
   p.dq_acc = dq_acc;
   p.dK = static_cast<__nv_bfloat16*>(dK);
   p.dV = static_cast<__nv_bfloat16*>(dV);
   p.num_items = B * Hkv * ((n + BM - 1) / BM);
+  // KV groups by expected work, largest first: the rows a key reaches grow
+  // with its heads' bin widths, which scale with sigma
+  p.ordered = 0;
+  const int G = Hq / Hkv;
+  if (Hkv <= kMaxOrder && (int)bn->sigma_host.size() == Hq) {
+    std::vector<double> cost(Hkv, 0.0);
+    for (int g = 0; g < Hkv; ++g)
+      for (int h = g * G; h < (g + 1) * G; ++h) cost[g] += 1.0 + bn->sigma_host[h] / BQ;
+    std::vector<int> order(Hkv);
+    std::iota(order.begin(), order.end(), 0);
+    std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return cost[a] > cost[b]; });
+    for (int g = 0; g < Hkv; ++g) p.kv_order[g] = order[g];
+    p.ordered = 1;
+  }
   p.queue = queue;
   p.err = err;
   p.wait_ns = wait_ns;
   const size_t smem = bwd_tc_smem_bytes();
   cudaError_t e = cudaMemsetAsync(dq_acc, 0, sizeof(float) * (size_t)B * Hq * n * HD, st);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, BwdTcParams) =
+      causal ? bwd_tc_kernel<true> : bwd_tc_kernel<false>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int grid = p.num_items < num_sms ? p.num_items : num_sms;
-  bwd_tc_kernel<<<grid, kThreads, smem, st>>>(mq, mk, mv, mdo, p);
+  kern<<<grid, kThreads, smem, st>>>(mq, mk, mv, mdo, macc, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t count4 = (int64_t)B * Hq * n * HD / 4;

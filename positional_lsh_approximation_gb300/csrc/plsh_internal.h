@@ -71,6 +71,12 @@ struct DeviceCtx {
   // per-chunk partial results of the decode step (m, l, P V), grown on demand
   float* decode_work = nullptr;
   size_t decode_work_bytes = 0;
+  cudaEvent_t decode_ev = nullptr;   // last stream use of decode_work
+  // scratch of the backward pass (row statistics, fp32 dQ accumulator),
+  // grown on demand and kept between calls
+  float* bwd_work = nullptr;
+  size_t bwd_work_bytes = 0;
+  cudaEvent_t bwd_ev = nullptr;      // last stream use of bwd_work
 };
 constexpr size_t kMaxTables = 16;
 constexpr int kQueueSlots = 1024;
