@@ -69,9 +69,10 @@ using namespace ptx;
 constexpr int BM = 128;                          // keys per tile (M of S^T)
 constexpr int BQ = 128;                          // queries per step
 constexpr int HD = 128;
-constexpr int kThreads = 192;
-constexpr int kProdWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kCompute = 256;                    // two warps per TMEM lane quarter
+constexpr int kThreads = kCompute + 64;
+constexpr int kProdWarp = 8;
+constexpr int kMmaWarp = 9;
 constexpr int kMaxG = 64;                        // query heads per KV head
 constexpr int kMaxSlotsB = 16;                   // bins kept per key thread
 constexpr int kMaxOrder = 64;                    // KV heads with a work order
@@ -182,7 +183,8 @@ __device__ __forceinline__ uint32_t row_mask(int a, int b) {
   return up & dn;
 }
 
-// Adds one step at the positions of `m` to a five-plane binary counter.
+// Adds one step at the positions of `m` to a five-plane binary counter (the
+// step count at each row, up to 31).
 __device__ __forceinline__ void plane_add5(uint32_t (&pl)[5], uint32_t m) {
 #pragma unroll
   for (int b = 0; b < 5; ++b) {
@@ -194,16 +196,21 @@ __device__ __forceinline__ void plane_add5(uint32_t (&pl)[5], uint32_t m) {
 
 // Multiplies the chunk's weights by the running count c(e): base plus the
 // steps at rows 1..e, up steps (bin starts, non-causal only) adding and dn
-// steps (bin ends) subtracting; one bit per step, four independent runs of
-// eight rows.
-template <bool UP>
-__device__ __forceinline__ void count_steps(float (&pv)[32], int base, uint32_t up, uint32_t dn) {
+// steps (bin ends) subtracting, the step counts held as P binary planes;
+// four independent runs of eight rows.
+template <bool UP, int P>
+__device__ __forceinline__ void count_planes(float (&pv)[32], int base, const uint32_t (&up)[5],
+                                             const uint32_t (&dn)[5]) {
   float c[4];
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
     const uint32_t le = (2u << (8 * g)) - 1u;    // rows 0 .. 8g
-    int cb = base - __popc(dn & le);
-    if (UP) cb += __popc(up & le);
+    int cb = base;
+#pragma unroll
+    for (int b = 0; b < P; ++b) {
+      cb -= __popc(dn[b] & le) << b;
+      if (UP) cb += __popc(up[b] & le) << b;
+    }
     c[g] = (float)cb;
   }
 #pragma unroll
@@ -212,32 +219,21 @@ __device__ __forceinline__ void count_steps(float (&pv)[32], int base, uint32_t 
     for (int g = 0; g < 4; ++g) {
       const int e = 8 * g + k;
       if (k > 0) {
-        if (dn & (1u << e)) c[g] -= 1.f;
-        if (UP && (up & (1u << e))) c[g] += 1.f;
+#pragma unroll
+        for (int b = 0; b < P; ++b) {
+          if (dn[b] & (1u << e)) c[g] -= (float)(1 << b);
+          if (UP && (up[b] & (1u << e))) c[g] += (float)(1 << b);
+        }
       }
       pv[e] *= c[g];
     }
   }
 }
 
-// The same with several steps at one row: binary planes of the step counts.
-template <bool UP>
-__device__ __forceinline__ void count_planes(float (&pv)[32], int base, const uint32_t (&up)[5],
-                                             const uint32_t (&dn)[5]) {
-#pragma unroll
-  for (int e = 0; e < 32; ++e) {
-    const uint32_t le = e == 31 ? 0xffffffffu : ((2u << e) - 1u);
-    int cb = base;
-#pragma unroll
-    for (int b = 0; b < 5; ++b) {
-      cb -= __popc(dn[b] & le) << b;
-      if (UP) cb += __popc(up[b] & le) << b;
-    }
-    pv[e] *= (float)cb;
-  }
-}
-
-template <bool CAUSAL>
+// SREG: register slots per key thread for its bins (s <= SREG; the slots past
+// s hold bins that count nowhere), a compile-time count so that the per-chunk
+// loop over them is unrolled without branches.
+template <bool CAUSAL, int SREG>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -260,19 +256,19 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     mbar_init(bar(B_KVEMPTY), 1);
     for (int k = 0; k < 2; ++k) {
       mbar_init(bar(B_QFULL + k), 1);
-      mbar_init(bar(B_QEMPTY + k), 4);           // the compute warps, once dQ staged there is read
+      mbar_init(bar(B_QEMPTY + k), 8);           // the compute warps, once dQ staged there is read
     }
     mbar_init(bar(B_DOFULL), 1);
     mbar_init(bar(B_DOEMPTY), 1);
     mbar_init(bar(B_SFULL), 1);
-    mbar_init(bar(B_PDS), BM);
+    mbar_init(bar(B_PDS), kCompute);
     mbar_init(bar(B_DQFULL), 1);
-    mbar_init(bar(B_DQEMPTY), BM);
+    mbar_init(bar(B_DQEMPTY), kCompute);
     mbar_init(bar(B_ACCFULL), 1);
-    mbar_init(bar(B_ACCEMPTY), BM);
+    mbar_init(bar(B_ACCEMPTY), kCompute);
     for (int k = 0; k < 2; ++k) {
       mbar_init(bar(B_IFULL + k), 1);
-      mbar_init(bar(B_IEMPTY + k), 1 + BM);      // the MMA thread and every compute thread
+      mbar_init(bar(B_IEMPTY + k), 1 + kCompute);   // the MMA thread and every compute thread
     }
     mbar_init(bar(B_DRAIN), 1);
     ctl->abort = 0;
@@ -592,16 +588,19 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     __syncwarp();
   } else {
     // ------------------------------------------------------------- compute
-    const int r = threadIdx.x;                   // TMEM lane: key row, or query row of dQ_p
+    // warps w and w + 4 share TMEM lanes 32 (w % 4) ...; ch = w / 4 picks the
+    // half of the query columns (of d for dQ_p, dV and dK) a warp handles
+    const int r = threadIdx.x & (BM - 1);        // TMEM lane: key row, or query row of dQ_p
+    const int ch = warp >> 2;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t t_s = tmem + lane_base, t_dp = t_s + 128, t_dv = t_s + 256, t_dk = t_s + 384;
     const float scale_log2 = kLog2e * 0.08838834764831845f;      // log2(e) / sqrt(128)
     const uint64_t scale2 = f2_pack(scale_log2, scale_log2);
     const uint32_t ds_row = sbase + OFF_DS + (uint32_t)r * 128u;  // this key's row of dS^T
     const int wq = warp & 3;
-    // the warp's rows of the two dS^T halves, 4 KB each (1024-byte aligned)
-    const uint32_t wpiece0 = sbase + OFF_DS + (uint32_t)wq * 4096u;
-    const uint32_t wpiece1 = wpiece0 + kHalf;
+    // the warp's rows of its dS^T half, 4 KB (1024-byte aligned): the only
+    // part of the dS buffer it writes
+    const uint32_t wpiece = sbase + OFF_DS + (uint32_t)ch * kHalf + (uint32_t)wq * 4096u;
     bool ok = true;
     int gstep = 0;
     for (int seq = 0; ok; ++seq) {
@@ -617,7 +616,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       int cur_h = -1;
       // this key's bins under the head's hashes, [lo_t, hi_t), and the rows
       // [ilo, ihi] that share at least one of them
-      int his[kMaxSlotsB], los[kMaxSlotsB];
+      int his[SREG], los[SREG];
       int ilo = 0, ihi = -1, himin = 0, lomax = 0;
       for (int k = 0; ok && k < it.steps; ++k, ++gstep) {
         int hg, qt;
@@ -633,7 +632,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           himin = INT_MAX;
           lomax = 0;
 #pragma unroll
-          for (int t = 0; t < kMaxSlotsB; ++t) {
+          for (int t = 0; t < SREG; ++t) {
             his[t] = CAUSAL ? -1 : (1 << 30);    // unused slots: no count, no step
             los[t] = 1 << 30;
             if (t < s) {
@@ -668,7 +667,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         __syncwarp();
         const int i0 = qt * BQ;
 #pragma unroll 1
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 2 * ch; q < 2 * ch + 2; ++q) {
           const int ic = i0 + q * 32;
           const uint32_t vm = row_mask(ilo - ic, ihi - ic);
           const uint32_t half = (uint32_t)(q >> 1);
@@ -689,57 +688,39 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           uint32_t sv32[32], dv32[32];
           tmem_ld32(t_s + q * 32, sv32);
           tmem_ld32(t_dp + q * 32, dv32);
-          // multiplicities over the chunk's rows: base at its first row,
-          // steps inside it
+          // multiplicities over the chunk's rows: the hashes whose bin
+          // around the key is open at its first row (base), and the number
+          // of bins that end (dn) or, not causal, start (up) at each row
+          // inside it, as binary planes; a step at a masked row only touches
+          // masked rows after it (vm is one run of rows), so it is dropped
           int base = s;
-          bool flat = true, multi = false;
+          int planes = 0;                          // warp-wide planes in use (0: flat)
           uint32_t up[5] = {0u, 0u, 0u, 0u, 0u}, dn[5] = {0u, 0u, 0u, 0u, 0u};
           const bool deep = himin > ic + 31 && (CAUSAL || lomax <= ic);
           if (!__all_sync(FULL, deep || vm == 0u)) {
-            int ch = 0, cl = 0;
-            uint32_t u0 = 0u, d0 = 0u, x0 = 0u;
+            int nh = 0, nl = 0;
 #pragma unroll
-            for (int t = 0; t < kMaxSlotsB; ++t) {
-              if (t >= s) break;
+            for (int t = 0; t < SREG; ++t) {
               const int dh = his[t] - ic;
-              ch += dh > 0 ? 1 : 0;
-              const uint32_t bh = shl_clamp(2u, dh - 1);
-              x0 |= d0 & bh;
-              d0 |= bh;
+              nh += dh > 0 ? 1 : 0;
+              plane_add5(dn, shl_clamp(2u, dh - 1) & vm);
               if (!CAUSAL) {
                 const int dl = los[t] - ic;
-                cl += dl > 0 ? 0 : 1;
-                const uint32_t bl = shl_clamp(2u, dl - 1);
-                x0 |= u0 & bl;
-                u0 |= bl;
+                nl += dl > 0 ? 0 : 1;
+                plane_add5(up, shl_clamp(2u, dl - 1) & vm);
               }
             }
-            base = CAUSAL ? ch : ch + cl - s;
-            if (vm == 0u) {
-              u0 = 0u;
-              d0 = 0u;
-              x0 = 0u;
-            }
-            up[0] = u0;
-            dn[0] = d0;
-            flat = (u0 | d0) == 0u;
-            multi = __any_sync(FULL, x0 != 0u);
-            if (multi) {
-              // several bin ends (or starts) at one row
-              up[0] = 0u;
-              dn[0] = 0u;
-              if (vm != 0u) {
-#pragma unroll
-                for (int t = 0; t < kMaxSlotsB; ++t) {
-                  if (t >= s) break;
-                  plane_add5(dn, shl_clamp(2u, his[t] - ic - 1));
-                  if (!CAUSAL) plane_add5(up, shl_clamp(2u, los[t] - ic - 1));
-                }
-              }
-            }
+            // not causal, a slot counts lo <= ic < hi as [hi > ic] + [lo <= ic] - 1
+            // (an unused one: 1 + 0 - 1)
+            base = CAUSAL ? nh : nh + nl - SREG;
+            planes = __any_sync(FULL, (dn[4] | up[4]) != 0u)   ? 5
+                     : __any_sync(FULL, (dn[3] | up[3]) != 0u) ? 4
+                     : __any_sync(FULL, (dn[2] | up[2]) != 0u) ? 3
+                     : __any_sync(FULL, (dn[1] | up[1]) != 0u) ? 2
+                     : __any_sync(FULL, (dn[0] | up[0]) != 0u) ? 1
+                                                               : 0;
           }
-          const bool all_flat = __all_sync(FULL, flat);
-          const float lgb = all_flat ? lg2((float)max(base, 1)) : 0.f;
+          const float lgb = planes == 0 ? lg2((float)max(base, 1)) : 0.f;
           const uint64_t lgb2 = f2_pack(lgb, lgb);
           tmem_wait_ld();
           float pv[32];
@@ -758,9 +739,13 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           }
 #pragma unroll
           for (int e = 0; e < 32; ++e) pv[e] = ex2(pv[e]);
-          if (!all_flat) {
-            if (multi) count_planes<!CAUSAL>(pv, base, up, dn);
-            else count_steps<!CAUSAL>(pv, base, up[0], dn[0]);
+          switch (planes) {
+            case 1: count_planes<!CAUSAL, 1>(pv, base, up, dn); break;
+            case 2: count_planes<!CAUSAL, 2>(pv, base, up, dn); break;
+            case 3: count_planes<!CAUSAL, 3>(pv, base, up, dn); break;
+            case 4: count_planes<!CAUSAL, 4>(pv, base, up, dn); break;
+            case 5: count_planes<!CAUSAL, 5>(pv, base, up, dn); break;
+            default: break;
           }
           uint32_t pk[16], dk[16];
 #pragma unroll
@@ -790,44 +775,38 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         tc_fence_before();
         mbar_arrive(bar(B_PDS));
         // this step's dQ rows (TMEM lane = query row) into the accumulator:
-        // each warp stages its 32 rows as four 128-byte swizzled fp32 boxes
-        // of 32 columns in the 4 KB pieces that hold its own rows of the dS
-        // buffer and of the step's Q buffer (both free once dQ_p has run),
-        // which TMA adds to the accumulator; the warp waits for the copy
-        // engine's reads only before it next writes there (the start of the
-        // next step, which also hands the Q buffer back)
+        // each warp stages its 32 rows and 64 of the d columns as two
+        // 128-byte swizzled fp32 boxes of 32 columns, one in its own piece
+        // of the dS buffer and one in its piece of the step's Q buffer (both
+        // free once dQ_p has run), which TMA adds to the accumulator; the
+        // warp waits for the copy engine's reads only before it next writes
+        // there (the start of the next step, which also hands the Q buffer
+        // back)
         ok = __all_sync(FULL, mbar_wait(bar(B_DQFULL), (uint32_t)gstep & 1u, abort, lim));
         if (!ok) break;
         tc_fence_after();
         {
           const int row0 = i0 + wq * 32;
           const int plane = it.b * p.Hq + h;
-          const uint32_t qpiece = sbase + OFF_Q + (uint32_t)(gstep & 1) * kTile + (uint32_t)wq * 4096u;
-#pragma unroll 1
-          for (int bx = 0; bx < 4; bx += 2) {
-            uint32_t o[64];
-            tmem_ld32(t_dp + bx * 32, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
-            tmem_ld32(t_dp + bx * 32 + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
-            tmem_wait_ld();
+          const uint32_t qpiece = sbase + OFF_Q + (uint32_t)(gstep & 1) * kTile +
+                                  (uint32_t)ch * kHalf + (uint32_t)wq * 4096u;
+          uint32_t o[64];
+          tmem_ld32(t_dp + ch * 64, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
+          tmem_ld32(t_dp + ch * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
+          tmem_wait_ld();
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int box = bx + u;
-              const uint32_t base = box == 0 ? wpiece0 : box == 1 ? wpiece1 : box == 2 ? qpiece
-                                                                                       : qpiece + kHalf;
-              const uint32_t row = base + (uint32_t)lane * 128u;
+          for (int u = 0; u < 2; ++u) {
+            const uint32_t row = (u == 0 ? wpiece : qpiece) + (uint32_t)lane * 128u;
 #pragma unroll
-              for (int c = 0; c < 8; ++c)
-                st_shared_v4(row + (((uint32_t)c ^ (uint32_t)(lane & 7)) << 4), o[32 * u + 4 * c],
-                             o[32 * u + 4 * c + 1], o[32 * u + 4 * c + 2], o[32 * u + 4 * c + 3]);
-            }
+            for (int c = 0; c < 8; ++c)
+              st_shared_v4(row + (((uint32_t)c ^ (uint32_t)(lane & 7)) << 4), o[32 * u + 4 * c],
+                           o[32 * u + 4 * c + 1], o[32 * u + 4 * c + 2], o[32 * u + 4 * c + 3]);
           }
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0 && row0 < n) {
-            tma_reduce_add_3d(&tmAcc, wpiece0, 0, row0, plane);
-            tma_reduce_add_3d(&tmAcc, wpiece1, 32, row0, plane);
-            tma_reduce_add_3d(&tmAcc, qpiece, 64, row0, plane);
-            tma_reduce_add_3d(&tmAcc, qpiece + kHalf, 96, row0, plane);
+            tma_reduce_add_3d(&tmAcc, wpiece, ch * 64, row0, plane);
+            tma_reduce_add_3d(&tmAcc, qpiece, ch * 64 + 32, row0, plane);
             bulk_commit();
           }
         }
@@ -842,7 +821,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       if (it.steps > 0) {
         const int64_t krow = ((int64_t)it.b * p.Hkv + it.kvh) * n + j;
 #pragma unroll 1
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 2 * ch; q < 2 * ch + 2; ++q) {
           uint32_t a[32], g[32];
           tmem_ld32(t_dv + q * 32, a);
           tmem_ld32(t_dk + q * 32, g);
@@ -868,9 +847,9 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       } else if (key_ok) {
         // no query row shares a bin with this key: zero gradients
         const int64_t krow = ((int64_t)it.b * p.Hkv + it.kvh) * n + j;
-        uint4* ov = reinterpret_cast<uint4*>(p.dV + krow * HD);
-        uint4* ok4 = reinterpret_cast<uint4*>(p.dK + krow * HD);
-        for (int v = 0; v < HD / 8; ++v) ov[v] = ok4[v] = make_uint4(0u, 0u, 0u, 0u);
+        uint4* ov = reinterpret_cast<uint4*>(p.dV + krow * HD + ch * 64);
+        uint4* ok4 = reinterpret_cast<uint4*>(p.dK + krow * HD + ch * 64);
+        for (int v = 0; v < 8; ++v) ov[v] = ok4[v] = make_uint4(0u, 0u, 0u, 0u);
       }
       tc_fence_before();
       mbar_arrive(bar(B_ACCEMPTY));
@@ -883,7 +862,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   }
 
   // the accumulator's reductions are complete before the CTA exits
-  if (warp < 4 && lane == 0) bulk_wait_all();
+  if (warp < kCompute / 32 && lane == 0) bulk_wait_all();
   tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {
@@ -986,8 +965,17 @@ cudaError_t launch_attn_bwd_tc(const void* Q, const void* K, const void* V, cons
   const size_t smem = bwd_tc_smem_bytes();
   cudaError_t e = cudaMemsetAsync(dq_acc, 0, sizeof(float) * (size_t)B * Hq * n * HD, st);
   if (e != cudaSuccess) return e;
-  void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, BwdTcParams) =
-      causal ? bwd_tc_kernel<true> : bwd_tc_kernel<false>;
+  using Kern = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
+                        BwdTcParams);
+  const int sreg = p.s <= 4 ? 4 : p.s <= 8 ? 8 : p.s <= 10 ? 10 : p.s <= 12 ? 12 : 16;
+  Kern kern = nullptr;
+  switch (sreg) {
+    case 4: kern = causal ? bwd_tc_kernel<true, 4> : bwd_tc_kernel<false, 4>; break;
+    case 8: kern = causal ? bwd_tc_kernel<true, 8> : bwd_tc_kernel<false, 8>; break;
+    case 10: kern = causal ? bwd_tc_kernel<true, 10> : bwd_tc_kernel<false, 10>; break;
+    case 12: kern = causal ? bwd_tc_kernel<true, 12> : bwd_tc_kernel<false, 12>; break;
+    default: kern = causal ? bwd_tc_kernel<true, 16> : bwd_tc_kernel<false, 16>; break;
+  }
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int grid = p.num_items < num_sms ? p.num_items : num_sms;

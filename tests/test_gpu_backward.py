@@ -34,6 +34,14 @@ CASES = [
      (1.2, 6.0, 40.0, 300.0, 2.0, 9.0, 70.0, 500.0)),
     ("tc_causal_s16", 1, 2, 1, 700, 128, "bf16", True, 16, (4.0, 120.0)),
     ("tc_one_tile", 1, 2, 2, 100, 128, "bf16", True, 3, (2.0, 1e4)),
+    # every register-slot variant of the kernel (s <= 4, 8, 10, 12, 16), and
+    # sigma far below one position, where many bins of a key end on one row
+    ("tc_noncausal_s3", 1, 2, 2, 260, 128, "bf16", False, 3, (1.5, 30.0)),
+    ("tc_noncausal_s10", 1, 2, 1, 390, 128, "bf16", False, 10, (0.9, 45.0)),
+    ("tc_causal_s12", 1, 4, 2, 450, 128, "bf16", True, 12, (0.6, 5.0, 30.0, 200.0)),
+    ("tc_noncausal_s12", 1, 2, 1, 300, 128, "bf16", False, 12, (2.5, 70.0)),
+    ("tc_noncausal_s16", 1, 2, 2, 280, 128, "bf16", False, 16, (0.4, 12.0)),
+    ("tc_causal_tiny_sigma", 1, 2, 1, 300, 128, "bf16", True, 16, (0.3, 0.8)),
 ]
 
 
