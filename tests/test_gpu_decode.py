@@ -66,6 +66,10 @@ CASES = [
     ("f32_d64_s64", 1, 2, 1, 800, 64, "f32", 64, (1.5, 40.0), [799, 300]),
     # one bin over the whole prefix: the envelope spans five 512-key chunks
     ("bf16_one_bin", 1, 2, 1, 2100, 128, "bf16", 3, (1e5, 1e5), [2099, 1536]),
+    # three heads per KV group (two warps each, two idle), and twelve (two
+    # CTAs per group: eight heads and four)
+    ("bf16_g3", 2, 3, 1, 900, 128, "bf16", 4, (5.0, 60.0, 500.0), [899, 450, 63, 64]),
+    ("bf16_g12", 1, 24, 2, 700, 128, "bf16", 5, (), [699, 100]),
 ]
 
 
