@@ -518,7 +518,10 @@ def measure_backward(w, bins, Q, K, V, f_block, flush, stream, iters=5):
     path (a forward pass in its row statistics mode, the backward kernel,
     the dQ conversion) against its roofline, the paper's block work of the
     backward (S, dP, dV, dK, dQ: 10 d per block pair, 2.5 x the forward's
-    F_block) at the bf16 peak; and the CUDA-core path on the same call."""
+    F_block) at the bf16 peak; the same from the forward's saved O and
+    log-sum-exp (the rows' Delta from O instead of a forward recomputation),
+    with the forward that writes them; and the CUDA-core path on the same
+    call."""
     import torch
     import positional_lsh_approximation_gb300 as plsh
     g = torch.Generator(device=Q.device)
@@ -526,6 +529,13 @@ def measure_backward(w, bins, Q, K, V, f_block, flush, stream, iters=5):
     dO = torch.randn(Q.shape, generator=g, device=Q.device).to(Q.dtype)
     run = lambda: plsh.alibi_attn_backward(Q, K, V, dO, bins, w.causal)
     t = time_calls(run, flush, stream, iters)
+    plsh.stream_status()
+    # from the forward's saved O and log-sum-exp, as a training step has them
+    O, lse = plsh.alibi_attn_lse(Q, K, V, bins, w.causal)
+    t_fwd_lse = time_calls(lambda: plsh.alibi_attn_lse(Q, K, V, bins, w.causal, out=O, lse=lse),
+                           flush, stream, iters)
+    t_saved = time_calls(lambda: plsh.alibi_attn_backward_lse(Q, K, V, O, lse, dO, bins, w.causal),
+                         flush, stream, iters)
     plsh.stream_status()
     os.environ["PLSH_PATH"] = "simt"
     try:
@@ -538,6 +548,9 @@ def measure_backward(w, bins, Q, K, V, f_block, flush, stream, iters=5):
     return {"path": plsh.attn_path(Q, bins, w.causal), "ms": t,
             "tokens_per_s": w.B * w.n / (t / 1e3), "flops_per_call": f_bwd,
             "tensor_frac": f_bwd / (t / 1e3) / 1e12 / pk["bf16_tflops"],
+            "from_saved_lse_ms": t_saved,
+            "from_saved_lse_tensor_frac": f_bwd / (t_saved / 1e3) / 1e12 / pk["bf16_tflops"],
+            "forward_with_lse_ms": t_fwd_lse,
             "cuda_core_ms": t_simt,
             "kernels": "attn_tc_kernel (row statistics) + bwd_tc_kernel + dq_convert_kernel"}
 

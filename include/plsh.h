@@ -163,6 +163,23 @@ plsh_status plsh_alibi_attn_backward(const plsh_tensor* Q, const plsh_tensor* K,
                                      plsh_tensor* dK, plsh_tensor* dV, void* stream);
 
 /*
+ * plsh_alibi_attn_backward_lse -- the same gradients from the forward pass's
+ * output O and log-sum-exp lse (written by plsh_alibi_attn_lse for the same
+ * Q, K, V, bins and causal), as a training step has them: the rows'
+ * Delta_i = dO_i . O_i comes from O (bf16, as stored) in a pass over the rows
+ * instead of a recomputation of the forward pass.
+ *   O [B,Hq,n,d] with Q's shape and dtype; lse [B*Hq*n] fp32 device memory.
+ * Tensor cores only (bf16, d = 128, s <= 16, Hq / Hkv <= 64): other inputs
+ * return PLSH_ERR_UNSUPPORTED.  Scratch, ordering and errors as for
+ * plsh_alibi_attn_backward.  Asynchronous on `stream`.
+ */
+plsh_status plsh_alibi_attn_backward_lse(const plsh_tensor* Q, const plsh_tensor* K,
+                                         const plsh_tensor* V, const plsh_tensor* O,
+                                         const float* lse, const plsh_tensor* dO,
+                                         const plsh_bins* bins, int32_t causal, plsh_tensor* dQ,
+                                         plsh_tensor* dK, plsh_tensor* dV, void* stream);
+
+/*
  * plsh_bias_error -- the bias of the averaged mask for head h of `bins`:
  * ||L* - M~||_max and ||L* - M~||_2 with L*_ij = e^{-|i-j|/sigma} (Problem
  * statement) and M~ = (1/s) sum_t M(h_t) (Methodology 1-2), the two norms the
@@ -244,6 +261,21 @@ void plsh_bins_free(plsh_bins* bins);
 plsh_status plsh_alibi_attn(const plsh_tensor* Q, const plsh_tensor* K,
                             const plsh_tensor* V, const plsh_bins* bins,
                             int32_t causal, plsh_tensor* O, void* stream);
+
+/*
+ * plsh_alibi_attn_lse -- plsh_alibi_attn that also writes every row's
+ * base-2 log-sum-exp of its scaled scores with their multiplicities,
+ *   lse_i = log2 sum_j c_ij 2^{x_ij},  x_ij = q_i . k_j log2(e) / sqrt(d)
+ * (so that T~_i = sum_j c_ij 2^{x_ij - lse_i} v_j), the statistic the backward
+ * pass needs (plsh_alibi_attn_backward_lse).
+ *   lse [B*Hq*n] fp32 device memory, row (b, h, i) at (b*Hq + h)*n + i.
+ * Tensor-core path only (bf16, d = 128, s within its budget; plsh_attn_path):
+ * other inputs return PLSH_ERR_UNSUPPORTED.  O as for plsh_alibi_attn.
+ * Asynchronous on `stream`.
+ */
+plsh_status plsh_alibi_attn_lse(const plsh_tensor* Q, const plsh_tensor* K,
+                                const plsh_tensor* V, const plsh_bins* bins, int32_t causal,
+                                plsh_tensor* O, float* lse, void* stream);
 
 /*
  * plsh_alibi_attn_noalloc -- plsh_alibi_attn for callers that may not

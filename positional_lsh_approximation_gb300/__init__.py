@@ -84,6 +84,8 @@ def load():
             "plsh_bins_share_groups": [P, I32, P, ctypes.POINTER(P)],
             "plsh_bias_error": [P, ctypes.c_double, I32, I32, U64, D, D, P],
             "plsh_alibi_attn_backward": [TP, TP, TP, TP, P, I32, TP, TP, TP, P],
+            "plsh_alibi_attn_backward_lse": [TP, TP, TP, TP, P, TP, P, I32, TP, TP, TP, P],
+            "plsh_alibi_attn_lse": [TP, TP, TP, P, I32, TP, P, P],
             "plsh_alibi_attn": [TP, TP, TP, P, I32, TP, P],
             "plsh_alibi_attn_noalloc": [TP, TP, TP, P, I32, TP, P],
             "plsh_alibi_attn_host": [TP, TP, TP, P, I32, TP, P],
@@ -290,6 +292,19 @@ def alibi_attn(Q, K, V, bins: Bins, causal: bool, out=None, stream=None):
     return _run(load().plsh_alibi_attn, Q, K, V, bins.handle, causal, out, stream)
 
 
+def alibi_attn_lse(Q, K, V, bins: Bins, causal: bool, out=None, lse=None, stream=None):
+    """plsh_alibi_attn_lse: (O, lse), lse [B*Hq*n] fp32 the rows' base-2
+    log-sum-exp (device tensors, tensor-core path)."""
+    O = torch.empty_like(Q) if out is None else out
+    L = torch.empty(Q.shape[0] * Q.shape[1] * Q.shape[2], dtype=torch.float32,
+                    device=Q.device) if lse is None else lse
+    tq, tk, tv, to = _desc(Q), _desc(K), _desc(V), _desc(O)
+    _check(load().plsh_alibi_attn_lse(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv),
+                                      bins.handle, int(bool(causal)), ctypes.byref(to),
+                                      ctypes.c_void_p(L.data_ptr()), _stream(stream)))
+    return O, L
+
+
 def alibi_attn_noalloc(Q, K, V, bins: Bins, causal: bool, out=None, stream=None):
     """plsh_alibi_attn_noalloc: plsh_alibi_attn without any device allocation
     inside the call (fixed scratch compiled into the library)."""
@@ -324,6 +339,20 @@ def alibi_attn_backward(Q, K, V, dO, bins: Bins, causal: bool, stream=None):
         ctypes.byref(t[0]), ctypes.byref(t[1]), ctypes.byref(t[2]), ctypes.byref(t[3]),
         bins.handle, int(bool(causal)), ctypes.byref(t[4]), ctypes.byref(t[5]),
         ctypes.byref(t[6]), _stream(stream)))
+    return dQ, dK, dV
+
+
+def alibi_attn_backward_lse(Q, K, V, O, lse, dO, bins: Bins, causal: bool, stream=None):
+    """plsh_alibi_attn_backward_lse: (dQ, dK, dV) from the forward's O and lse
+    (alibi_attn_lse), device tensors."""
+    if lse.dtype != torch.float32 or lse.numel() != Q.shape[0] * Q.shape[1] * Q.shape[2]:
+        raise ValueError("alibi_attn_backward_lse: lse must be float32 with B*Hq*n entries")
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    t = [_desc(x) for x in (Q, K, V, O, dO, dQ, dK, dV)]
+    _check(load().plsh_alibi_attn_backward_lse(
+        ctypes.byref(t[0]), ctypes.byref(t[1]), ctypes.byref(t[2]), ctypes.byref(t[3]),
+        ctypes.c_void_p(lse.data_ptr()), ctypes.byref(t[4]), bins.handle, int(bool(causal)),
+        ctypes.byref(t[5]), ctypes.byref(t[6]), ctypes.byref(t[7]), _stream(stream)))
     return dQ, dK, dV
 
 

@@ -499,7 +499,8 @@ Path path_override() {
 
 plsh_status run_attention(const plsh_tensor* Q, const plsh_tensor* K, const plsh_tensor* V,
                           plsh_tensor* O, int causal, const plsh_bins* bins,
-                          const float* slopes, cudaStream_t st, int qt0 = 0, int qt1 = -1) {
+                          const float* slopes, cudaStream_t st, int qt0 = 0, int qt1 = -1,
+                          float* lse = nullptr) {
   plsh::DeviceCtx* ctx = nullptr;
   plsh_status s0 = current_ctx(&ctx);
   if (s0 != PLSH_OK) return s0;
@@ -534,6 +535,10 @@ plsh_status run_attention(const plsh_tensor* Q, const plsh_tensor* K, const plsh
   if (path == Path::Tc && !tc_ok)
     return fail(PLSH_ERR_UNSUPPORTED, "tensor-core path needs bf16, d = 128 and s within "
                                       "its shared-memory budget");
+  if (lse != nullptr && path != Path::Tc)
+    return fail(PLSH_ERR_UNSUPPORTED, "the log-sum-exp output is written by the tensor-core "
+                                      "path only (bf16, d = 128)");
+  a.lse = lse;
   TableRef tab;
   if (path == Path::Tc) {
     const int QT = (int)((Q->n + 127) / 128);
@@ -551,7 +556,7 @@ plsh_status run_attention(const plsh_tensor* Q, const plsh_tensor* K, const plsh
                                    : plsh::launch_attn_simt(a, slopes, Q->dtype, st);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   if (path == Path::Tc && tab.merges > 0) {
-    e = plsh::launch_split_merge(tab.merge, tab.merges, tab.ws, a.O, a.Hq, a.n, st);
+    e = plsh::launch_split_merge(tab.merge, tab.merges, tab.ws, a.O, a.lse, a.Hq, a.n, st);
     if (e != cudaSuccess) return cuda_fail(e, "split merge launch");
   }
   return PLSH_OK;
@@ -762,12 +767,20 @@ plsh_status plsh_bins_fixed(int64_t n, const int32_t* width_h, int32_t H, int32_
   return PLSH_OK;
 }
 
-plsh_status plsh_alibi_attn_backward(const plsh_tensor* Q, const plsh_tensor* K,
-                                     const plsh_tensor* V, const plsh_tensor* dO,
-                                     const plsh_bins* bins, int32_t causal, plsh_tensor* dQ,
-                                     plsh_tensor* dK, plsh_tensor* dV, void* stream) {
+// The backward pass; O and lse (the forward's output and log-sum-exp) are
+// null when the row statistics are to be recomputed.
+plsh_status backward_impl(const plsh_tensor* Q, const plsh_tensor* K, const plsh_tensor* V,
+                          const plsh_tensor* O, const float* lse, const plsh_tensor* dO,
+                          const plsh_bins* bins, int32_t causal, plsh_tensor* dQ,
+                          plsh_tensor* dK, plsh_tensor* dV, void* stream) {
   plsh_status st = check_qkvo(Q, K, V, dO);
   if (st != PLSH_OK) return st;
+  if (O != nullptr) {
+    if ((st = check_tensor(O, "O")) != PLSH_OK) return st;
+    if (O->dtype != Q->dtype || O->B != Q->B || O->H != Q->H || O->n != Q->n || O->d != Q->d)
+      return fail(PLSH_ERR_INVALID, "O must have Q's shape and dtype");
+    if (lse == nullptr) return fail(PLSH_ERR_INVALID, "lse is NULL");
+  }
   if ((st = check_tensor(dQ, "dQ")) != PLSH_OK || (st = check_tensor(dK, "dK")) != PLSH_OK ||
       (st = check_tensor(dV, "dV")) != PLSH_OK)
     return st;
@@ -785,12 +798,17 @@ plsh_status plsh_alibi_attn_backward(const plsh_tensor* Q, const plsh_tensor* K,
   cudaStream_t cs = (cudaStream_t)stream;
   float* stats = nullptr;
   const size_t bytes = sizeof(float) * 3 * (size_t)Q->B * Q->H * Q->n;
-  if (bwd_tc_ok(Q, K, bins, causal ? 1 : 0)) {
-    // tensor cores: the forward kernel in its row statistics mode (m, l and
-    // Delta = dO . O per row, no output), then the backward kernel
+  const bool tc = bwd_tc_ok(Q, K, bins, causal ? 1 : 0);
+  if (O != nullptr && !tc)
+    return fail(PLSH_ERR_UNSUPPORTED, "the backward pass from a saved O and log-sum-exp runs on "
+                                      "the tensor cores only (bf16, d = 128, s <= 16)");
+  if (tc) {
+    // tensor cores: the rows' -lse and Delta = dO . O (from the saved O and
+    // lse, or from the forward kernel in its row statistics mode), then the
+    // backward kernel
     plsh::DeviceCtx* ctx = nullptr;
     if ((st = current_ctx(&ctx)) != PLSH_OK) return st;
-    const size_t stat_floats = ((bytes / sizeof(float)) + 63) & ~(size_t)63;
+    const size_t stat_floats = (2 * (size_t)Q->B * Q->H * Q->n + 63) & ~(size_t)63;
     const size_t acc_bytes = sizeof(float) * (size_t)Q->B * Q->H * Q->n * Q->d;
     std::lock_guard<std::mutex> bk(g_bwd_mu);
     if ((st = scratch_acquire(&ctx->bwd_work, &ctx->bwd_work_bytes, &ctx->bwd_ev,
@@ -835,11 +853,16 @@ plsh_status plsh_alibi_attn_backward(const plsh_tensor* Q, const plsh_tensor* K,
     if (s1 == PLSH_OK) {
       a.items = tab.items;
       a.num_items = tab.count;
-      e = plsh::launch_attn_tc(a, nullptr, ctx->num_sms, cs);
+      if (O != nullptr)
+        e = plsh::launch_bwd_delta(O->data, dO->data, lse, stats, dq_acc,
+                                   (int64_t)a.B * a.Hq * a.n, cs);
+      else
+        e = plsh::launch_attn_tc(a, nullptr, ctx->num_sms, cs);
       if (e == cudaSuccess)
         e = plsh::launch_attn_bwd_tc(Q->data, K->data, V->data, dO->data, dQ->data, dK->data,
-                                     dV->data, stats, dq_acc, bins, a.B, a.Hq, a.Hkv, a.n,
-                                     a.causal, bq, ctx->d_err, ctx->wait_ns, ctx->num_sms, cs);
+                                     dV->data, stats, dq_acc, O == nullptr, bins, a.B, a.Hq,
+                                     a.Hkv, a.n, a.causal, bq, ctx->d_err, ctx->wait_ns,
+                                     ctx->num_sms, cs);
     }
     const cudaError_t er = cudaEventRecord(ctx->bwd_ev, cs);
     if (s1 != PLSH_OK) return s1;
@@ -861,6 +884,22 @@ plsh_status plsh_alibi_attn_backward(const plsh_tensor* Q, const plsh_tensor* K,
   if (e == cudaSuccess) e = er;
   PLSH_TRY_CUDA(e, "backward launch");
   return PLSH_OK;
+}
+
+plsh_status plsh_alibi_attn_backward(const plsh_tensor* Q, const plsh_tensor* K,
+                                     const plsh_tensor* V, const plsh_tensor* dO,
+                                     const plsh_bins* bins, int32_t causal, plsh_tensor* dQ,
+                                     plsh_tensor* dK, plsh_tensor* dV, void* stream) {
+  return backward_impl(Q, K, V, nullptr, nullptr, dO, bins, causal, dQ, dK, dV, stream);
+}
+
+plsh_status plsh_alibi_attn_backward_lse(const plsh_tensor* Q, const plsh_tensor* K,
+                                         const plsh_tensor* V, const plsh_tensor* O,
+                                         const float* lse, const plsh_tensor* dO,
+                                         const plsh_bins* bins, int32_t causal, plsh_tensor* dQ,
+                                         plsh_tensor* dK, plsh_tensor* dV, void* stream) {
+  if (O == nullptr) return fail(PLSH_ERR_INVALID, "O is NULL");
+  return backward_impl(Q, K, V, O, lse, dO, bins, causal, dQ, dK, dV, stream);
 }
 
 plsh_status plsh_bias_error(const plsh_bins* bins, double sigma, int32_t h,
@@ -982,6 +1021,19 @@ plsh_status plsh_alibi_attn(const plsh_tensor* Q, const plsh_tensor* K, const pl
   if (bins->H != Q->H) return fail(PLSH_ERR_INVALID, "bins were drawn for another number of heads");
   if ((st = check_bins_device(bins)) != PLSH_OK) return st;
   return run_attention(Q, K, V, O, causal, bins, nullptr, (cudaStream_t)stream);
+}
+
+plsh_status plsh_alibi_attn_lse(const plsh_tensor* Q, const plsh_tensor* K, const plsh_tensor* V,
+                                const plsh_bins* bins, int32_t causal, plsh_tensor* O, float* lse,
+                                void* stream) {
+  plsh_status st = check_qkvo(Q, K, V, O);
+  if (st != PLSH_OK) return st;
+  if (lse == nullptr) return fail(PLSH_ERR_INVALID, "lse is NULL");
+  if (bins == nullptr) return fail(PLSH_ERR_INVALID, "bins is NULL");
+  if (bins->n != Q->n) return fail(PLSH_ERR_INVALID, "bins were drawn for another n");
+  if (bins->H != Q->H) return fail(PLSH_ERR_INVALID, "bins were drawn for another number of heads");
+  if ((st = check_bins_device(bins)) != PLSH_OK) return st;
+  return run_attention(Q, K, V, O, causal, bins, nullptr, (cudaStream_t)stream, 0, -1, lse);
 }
 
 plsh_status plsh_alibi_attn_host(const plsh_tensor* Q, const plsh_tensor* K,

@@ -782,10 +782,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
           }
         }
         if (valid) {
-          float* st3 = a.stats + (row0 + i) * 3;
-          st3[0] = pend_m;
-          st3[1] = pend_l;
-          st3[2] = dsum * inv_l;
+          float* st2 = a.stats + (row0 + i) * 2;
+          st2[0] = pend_l > 0.f ? -(pend_m + lg2(pend_l)) : -INFINITY;
+          st2[1] = dsum * inv_l;
         }
         if (a.O == nullptr) {
           tc_fence_before();
@@ -793,6 +792,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
           pend = false;
           return true;
         }
+      } else if (a.lse != nullptr && qt >= 0 && i < n) {
+        a.lse[row0 + i] = pend_l > 0.f ? pend_m + lg2(pend_l) : -INFINITY;
       }
 #pragma unroll 1
       for (int q2 = 0; q2 < 2; ++q2) {
@@ -1341,7 +1342,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
 // of the head dimension per lane.  Grid: (split items, 2 tiles, 16 row groups).
 __global__ void __launch_bounds__(256)
 split_merge_kernel(const int4* __restrict__ merge, const float* __restrict__ ws,
-                   __nv_bfloat16* __restrict__ O, int Hq, int n) {
+                   __nv_bfloat16* __restrict__ O, float* __restrict__ lse, int Hq, int n) {
   const int item = blockIdx.x, tile = blockIdx.y;
   const int r = blockIdx.z * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   const int4 e = merge[2 * item], x = merge[2 * item + 1];
@@ -1376,6 +1377,8 @@ split_merge_kernel(const int4* __restrict__ merge, const float* __restrict__ ws,
       reinterpret_cast<__nv_bfloat162*>(O + (((int64_t)e.x * Hq + h) * n + i) * HD) + 2 * lane;
   out[0] = __floats2bfloat162_rn(o.x * inv, o.y * inv);
   out[1] = __floats2bfloat162_rn(o.z * inv, o.w * inv);
+  if (lse != nullptr && lane == 0)
+    lse[((int64_t)e.x * Hq + h) * n + i] = l > 0.f ? m + __log2f(l) : -INFINITY;
 }
 
 // ------------------------------------------------------------------- host
@@ -1477,11 +1480,11 @@ size_t attn_tc_smem_bytes(int s, int causal, int exact) {
   return smem_for(kSlots, out_staged(s, causal, exact), s, causal, exact);
 }
 
-cudaError_t launch_split_merge(const int4* merge, int count, const float* ws, void* O, int Hq,
-                               int n, cudaStream_t st) {
+cudaError_t launch_split_merge(const int4* merge, int count, const float* ws, void* O, float* lse,
+                               int Hq, int n, cudaStream_t st) {
   if (count <= 0) return cudaSuccess;
   split_merge_kernel<<<dim3((unsigned)count, 2, BM / 8), 256, 0, st>>>(
-      merge, ws, static_cast<__nv_bfloat16*>(O), Hq, n);
+      merge, ws, static_cast<__nv_bfloat16*>(O), lse, Hq, n);
   return cudaGetLastError();
 }
 

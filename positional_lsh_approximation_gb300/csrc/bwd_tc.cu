@@ -112,7 +112,7 @@ struct BwdTcParams {
   int s;
   int64_t W;
   int B, Hq, Hkv, n;
-  const float* stats;                            // [B * Hq * n][3]
+  const float* stats;                            // [B * Hq * n][2]: -lse, Delta
   float* dq_acc;                                 // [B * Hq * n][128] fp32, zeroed
   __nv_bfloat16* dK;                             // [B, Hkv, n, 128]
   __nv_bfloat16* dV;
@@ -392,7 +392,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       }
       ok = __shfl_sync(FULL, (int)ok, 0) != 0;
       // the rows' statistics of the next step, read ahead into registers
-      float sm[4], sl[4], sd[4];
+      float sm[4], sd[4];
       uint4 rr[2];
       auto load_stats = [&](int k) {
         int hg, qt;
@@ -411,14 +411,12 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int i = qt * BQ + u * 32 + lane;
-          sm[u] = 0.f;
-          sl[u] = 0.f;
+          sm[u] = -INFINITY;
           sd[u] = 0.f;
           if (i < n) {
-            const float* st = p.stats + (rowbase + i) * 3;
-            sm[u] = __ldg(st);
-            sl[u] = __ldg(st + 1);
-            sd[u] = __ldg(st + 2);
+            const float2 st = __ldg(reinterpret_cast<const float2*>(p.stats) + rowbase + i);
+            sm[u] = st.x;
+            sd[u] = st.y;
           }
         }
       };
@@ -450,7 +448,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int r = u * 32 + lane;
-          sv[r] = sl[u] > 0.f ? -(sm[u] + lg2(sl[u])) : -INFINITY;
+          sv[r] = sm[u];
           sv[BQ + r] = sd[u];
         }
         uint4* rv = &ctl->recs[gstep & 1][0][0];
@@ -879,6 +877,26 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   }
 }
 
+// The rows' statistics from a saved O and its base-2 log-sum-exp: (-lse,
+// Delta = dO . O) per row, and the row of the dQ accumulator cleared.  A warp
+// per row, four values of the head dimension per lane.
+__global__ void __launch_bounds__(256)
+bwd_delta_kernel(const uint2* __restrict__ O, const uint2* __restrict__ dO,
+                 const float* __restrict__ lse, float2* __restrict__ stats,
+                 float4* __restrict__ acc, int64_t rows) {
+  const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const uint2 o = O[row * 32 + lane], g = dO[row * 32 + lane];
+  float d = __uint_as_float(o.x << 16) * __uint_as_float(g.x << 16);
+  d = fmaf(__uint_as_float(o.x & 0xffff0000u), __uint_as_float(g.x & 0xffff0000u), d);
+  d = fmaf(__uint_as_float(o.y << 16), __uint_as_float(g.y << 16), d);
+  d = fmaf(__uint_as_float(o.y & 0xffff0000u), __uint_as_float(g.y & 0xffff0000u), d);
+  for (int k = 16; k > 0; k >>= 1) d += __shfl_xor_sync(FULL, d, k);
+  acc[row * 32 + lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (lane == 0) stats[row] = make_float2(-lse[row], d);
+}
+
 // dQ = dq_acc / sqrt(128) in bf16
 __global__ void dq_convert_kernel(const float4* __restrict__ acc, uint2* __restrict__ out,
                                   int64_t count4) {
@@ -920,10 +938,19 @@ bool make_acc_map(CUtensorMap* map, float* base, int64_t planes, int64_t n) {
 
 size_t bwd_tc_smem_bytes() { return 1024 + OFF_END + sizeof(CtlB); }
 
+cudaError_t launch_bwd_delta(const void* O, const void* dO, const float* lse, float* stats,
+                             float* dq_acc, int64_t rows, cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  bwd_delta_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(
+      static_cast<const uint2*>(O), static_cast<const uint2*>(dO), lse,
+      reinterpret_cast<float2*>(stats), reinterpret_cast<float4*>(dq_acc), rows);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_attn_bwd_tc(const void* Q, const void* K, const void* V, const void* dO,
                                void* dQ, void* dK, void* dV, const float* stats, float* dq_acc,
-                               const plsh_bins* bn, int B, int Hq, int Hkv, int n, int causal,
-                               int* queue, int* err, uint64_t wait_ns, int num_sms,
+                               bool clear_acc, const plsh_bins* bn, int B, int Hq, int Hkv, int n,
+                               int causal, int* queue, int* err, uint64_t wait_ns, int num_sms,
                                cudaStream_t st) {
   CUtensorMap mq, mk, mv, mdo, macc;
   if (!make_tile_map_bf16(&mq, Q, (int64_t)B * Hq, n) ||
@@ -963,7 +990,8 @@ cudaError_t launch_attn_bwd_tc(const void* Q, const void* K, const void* V, cons
   p.err = err;
   p.wait_ns = wait_ns;
   const size_t smem = bwd_tc_smem_bytes();
-  cudaError_t e = cudaMemsetAsync(dq_acc, 0, sizeof(float) * (size_t)B * Hq * n * HD, st);
+  cudaError_t e = cudaSuccess;
+  if (clear_acc) e = cudaMemsetAsync(dq_acc, 0, sizeof(float) * (size_t)B * Hq * n * HD, st);
   if (e != cudaSuccess) return e;
   using Kern = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
                         BwdTcParams);

@@ -125,11 +125,14 @@ struct AttnArgs {
   const int4* item_ext;            // split parts {part, parts, slot, 0}, or null
   float* split_ws;                 // workspace slots of split parts
   // row statistics mode (the backward pass's first step): with stats set,
-  // every row's running max m (log2 units of the scaled scores), row sum l
-  // and Delta = sum_d O_d dO_d (O = acc / l in fp32) go to stats[row][3],
-  // with dO [B, Hq, n, 128] bf16; O itself is written only when O != null
+  // every row's -lse (lse = m + log2 l, the base-2 log-sum-exp of the scaled
+  // scores with their multiplicities; m the running max, l the row sum) and
+  // Delta = sum_d O_d dO_d (O = acc / l in fp32) go to stats[row][2], with
+  // dO [B, Hq, n, 128] bf16; O itself is written only when O != null
   float* stats;
   const void* dO;
+  // with lse set (and no stats), every row's lse goes to lse[row] beside O
+  float* lse;
   int* err;
   int* queue;                      // {next item, finished CTAs}
   uint64_t wait_ns;
@@ -177,23 +180,29 @@ cudaError_t launch_attn_tc(const AttnArgs& a, const float* slopes_host,
                            int num_sms, cudaStream_t st);
 // combines the parts of `count` split items (entries of `merge`, two int4
 // each) into O (bf16 [B, Hq, n, 128])
-cudaError_t launch_split_merge(const int4* merge, int count, const float* ws, void* O, int Hq,
-                               int n, cudaStream_t st);
+cudaError_t launch_split_merge(const int4* merge, int count, const float* ws, void* O, float* lse,
+                               int Hq, int n, cudaStream_t st);
 size_t attn_tc_smem_bytes(int s, int causal, int exact);
 // [planes, n, 128] bf16 as a TMA tensor map with 64 x 128 x 1 boxes, 128-byte
 // swizzle, rows past n reading as zeros (attn_tc.cu)
 bool make_tile_map_bf16(CUtensorMap* map, const void* base, int64_t planes, int64_t n);
 
 // bwd_tc.cu: gradients on the tensor cores (bf16, d = 128, s <= 16) from the
-// rows' statistics [B * Hq * n][3] (m, l, Delta); dq_acc is fp32 scratch of
-// B * Hq * n * 128 floats, zeroed by the call
+// rows' statistics [B * Hq * n][2] (-lse, Delta); dq_acc is fp32 scratch of
+// B * Hq * n * 128 floats, cleared by the call when clear_acc is set (else
+// already zero)
 constexpr int kBwdTcMaxS = 16;
 constexpr int kBwdTcMaxGroup = 64;
 size_t bwd_tc_smem_bytes();
 cudaError_t launch_attn_bwd_tc(const void* Q, const void* K, const void* V, const void* dO,
                                void* dQ, void* dK, void* dV, const float* stats, float* dq_acc,
-                               const plsh_bins* bn, int B, int Hq, int Hkv, int n, int causal,
-                               int* queue, int* err, uint64_t wait_ns, int num_sms,
+                               bool clear_acc, const plsh_bins* bn, int B, int Hq, int Hkv, int n,
+                               int causal, int* queue, int* err, uint64_t wait_ns, int num_sms,
                                cudaStream_t st);
+// the rows' statistics from a saved O and lse ([rows] base-2 log-sum-exp):
+// stats[row] = (-lse, dO . O), and dq_acc's rows cleared (rows = B * Hq * n,
+// O and dO [rows][128] bf16)
+cudaError_t launch_bwd_delta(const void* O, const void* dO, const float* lse, float* stats,
+                             float* dq_acc, int64_t rows, cudaStream_t st);
 
 }  // namespace plsh

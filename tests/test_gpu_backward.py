@@ -90,3 +90,67 @@ def test_tensor_core_backward_agrees_with_cuda_cores(monkeypatch):
         scale = np.abs(b).max()
         assert np.abs(a - b).max() <= 1.5e-2 * scale, what
     bins.free()
+
+
+LSE_CASES = [
+    # name, B, Hq, Hkv, n, causal, s, sigma, split parts
+    ("causal_gqa", 1, 4, 2, 700, True, 10, (1.5, 8.0, 60.0, 400.0), 0),
+    ("noncausal", 2, 2, 1, 390, False, 6, (3.0, 90.0), 0),
+    ("causal_split3", 1, 2, 1, 900, True, 8, (300.0, 2000.0), 3),
+]
+
+
+def _lse_inputs(case):
+    name, B, Hq, Hkv, n, causal, s, sig, parts = case
+    w = Workload(name, B, Hq, Hkv, n, 128, "bf16", causal, s, sig, qkv_seed=n + 11)
+    Q, K, V = make_qkv(w)
+    dev = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(torch.bfloat16).cuda()
+    return w, Q, K, V, dev
+
+
+@pytest.mark.parametrize("case", LSE_CASES, ids=[c[0] for c in LSE_CASES])
+def test_forward_lse_matches_oracle(case):
+    """O from plsh_alibi_attn_lse is the O of plsh_alibi_attn, bit for bit,
+    and lse_i = log2 of the oracle's unshifted row sum sum_j c_ij e^{S_ij}."""
+    w, Q, K, V, dev = _lse_inputs(case)
+    parts = case[-1]
+    bins = plsh.sample_bins(w.n, w.sigmas(), w.s, seed=3)
+    off, st = oracle.sample_bins(w.n, w.sigmas(), w.s, seed=3)
+    plsh.set_split_parts(parts)
+    try:
+        O, lse = plsh.alibi_attn_lse(dev(Q), dev(K), dev(V), bins, w.causal)
+        O2 = plsh.alibi_attn(dev(Q), dev(K), dev(V), bins, w.causal)
+        plsh.stream_status()
+    finally:
+        plsh.set_split_parts(0)
+    assert torch.equal(O, O2)
+    rows = oracle.all_rows(w.B, w.Hq, w.n)
+    _, den = oracle.plsh_parts_rows(Q, K, V, off, st, w.s, w.causal, rows)
+    want = np.log2(den)
+    got = lse.cpu().numpy().astype(np.float64)
+    err = np.abs(got - want).max()
+    assert err <= 2e-3, f"{case[0]}: lse max err {err:.3e}"
+    bins.free()
+
+
+@pytest.mark.parametrize("case", LSE_CASES[:2], ids=[c[0] for c in LSE_CASES[:2]])
+def test_backward_from_saved_lse_matches_oracle(case):
+    """Gradients from the forward's O and lse against the oracle's, and
+    against the recomputing backward pass."""
+    w, Q, K, V, dev = _lse_inputs(case)
+    dO = np.random.default_rng(w.n).standard_normal(Q.shape).astype(np.float32)
+    dO = torch.from_numpy(dO).to(torch.bfloat16).float().numpy()
+    bins = plsh.sample_bins(w.n, w.sigmas(), w.s, seed=3)
+    off, st = oracle.sample_bins(w.n, w.sigmas(), w.s, seed=3)
+    q, k, v, do = dev(Q), dev(K), dev(V), dev(dO)
+    O, lse = plsh.alibi_attn_lse(q, k, v, bins, w.causal)
+    saved = plsh.alibi_attn_backward_lse(q, k, v, O, lse, do, bins, w.causal)
+    recomputed = plsh.alibi_attn_backward(q, k, v, do, bins, w.causal)
+    plsh.stream_status()
+    ref = oracle.plsh_attn_backward(Q, K, V, dO, off, st, w.s, w.causal)
+    for got, again, want, what in zip(saved, recomputed, ref, ("dQ", "dK", "dV")):
+        g = got.float().cpu().numpy().astype(np.float64)
+        scale = np.abs(want).max()
+        assert np.abs(g - want).max() <= 1e-2 * scale, f"{case[0]} {what} vs oracle"
+        assert np.abs(g - again.float().cpu().numpy()).max() <= 1e-2 * scale, f"{case[0]} {what}"
+    bins.free()
