@@ -117,8 +117,15 @@ def _check(status: int):
         raise PlshError(status, lib.plsh_last_error().decode())
 
 
+# the current stream's raw handle without building a Stream object (the
+# lookup torch.cuda.current_stream() makes costs microseconds per call)
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream) -> ctypes.c_void_p:
     if stream is None:
+        if _raw_stream is not None:
+            return ctypes.c_void_p(_raw_stream(torch.cuda.current_device()))
         stream = torch.cuda.current_stream()
     if isinstance(stream, torch.cuda.Stream):
         return ctypes.c_void_p(stream.cuda_stream)

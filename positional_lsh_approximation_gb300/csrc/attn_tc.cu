@@ -1423,8 +1423,7 @@ cudaError_t launch_variant(const CUtensorMap& mq, const CUtensorMap& mk,
                            const CUtensorMap& mv, const TcParams& p,
                            size_t smem, int grid, cudaStream_t st) {
   auto kern = attn_tc_kernel<EXACT, CAUSAL, SREG>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), (int)smem);
   if (e != cudaSuccess) return e;
   // programmatic stream serialization: the CTAs may start (and set up
   // shared memory, barriers and TMEM) while the previous kernel finishes

@@ -1004,7 +1004,7 @@ cudaError_t launch_attn_bwd_tc(const void* Q, const void* K, const void* V, cons
     case 12: kern = causal ? bwd_tc_kernel<true, 12> : bwd_tc_kernel<false, 12>; break;
     default: kern = causal ? bwd_tc_kernel<true, 16> : bwd_tc_kernel<false, 16>; break;
   }
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  e = set_smem_limit(reinterpret_cast<const void*>(kern), (int)smem);
   if (e != cudaSuccess) return e;
   const int grid = p.num_items < num_sms ? p.num_items : num_sms;
   kern<<<grid, kThreads, smem, st>>>(mq, mk, mv, mdo, macc, p);

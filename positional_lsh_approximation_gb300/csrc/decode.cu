@@ -327,8 +327,7 @@ template <typename T, int D>
 cudaError_t launch_typed(const DecodeParams& p, void* out, cudaStream_t st) {
   using C = Cfg<T, D>;
   auto kern = decode_group_kernel<T, D>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)C::kSmem);
+  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), (int)C::kSmem);
   if (e != cudaSuccess) return e;
   const int64_t ctas = (int64_t)p.B * p.Hkv * p.hchunks * p.splits;
   kern<<<(unsigned)ctas, 32 * p.heads, C::kSmem, st>>>(p);

@@ -6,12 +6,32 @@
 #include <stdint.h>
 
 #include <map>
+#include <mutex>
 #include <string>
+#include <utility>
 #include <vector>
 
 #include "../../include/plsh.h"
 
 namespace plsh {
+
+// A kernel's dynamic shared-memory limit, set in the device's context the
+// first time a size is asked for (the attribute persists), so that repeated
+// launches skip the driver call.
+inline cudaError_t set_smem_limit(const void* kern, int bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<int, const void*>, int> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(mu);
+  int& have = done[std::make_pair(dev, kern)];
+  if (have >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) have = bytes;
+  return e;
+}
+
 
 // One record per (hash, 32-position word): which positions of the word open a
 // bin, the last bin start at or before the word's first position, and the
