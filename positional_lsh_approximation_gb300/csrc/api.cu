@@ -1160,9 +1160,15 @@ plsh_status plsh_alibi_decode(const plsh_tensor* q, const plsh_tensor* K, const 
   if ((st = check_bins_device(bins)) != PLSH_OK) return st;
   plsh::DeviceCtx* ctx = nullptr;
   if ((st = current_ctx(&ctx)) != PLSH_OK) return st;
+  double sigma_max = 1e30;                 // unknown scales: any envelope
+  if (bins->sigma_host.size() == (size_t)q->H) {
+    sigma_max = 0.0;
+    for (double sg : bins->sigma_host) sigma_max = sg > sigma_max ? sg : sigma_max;
+  }
+  const int useful = plsh::decode_useful_splits(sigma_max, (int)pos);
   const size_t bytes =
       sizeof(float) * plsh::decode_work_floats((int)q->B, (int)q->H, (int)K->H, (int)q->d,
-                                               ctx->num_sms);
+                                               ctx->num_sms, useful);
   std::lock_guard<std::mutex> dk(g_decode_mu);
   if ((st = scratch_acquire(&ctx->decode_work, &ctx->decode_work_bytes, &ctx->decode_ev, bytes,
                             (cudaStream_t)stream, "decode partials")) != PLSH_OK)
@@ -1184,6 +1190,7 @@ plsh_status plsh_alibi_decode(const plsh_tensor* q, const plsh_tensor* K, const 
   a.pos = (int)pos;
   a.dtype = q->dtype;
   a.num_sms = ctx->num_sms;
+  a.useful_splits = useful;
   a.work = work;
   a.err = ctx->d_err;
   a.wait_ns = ctx->wait_ns;

@@ -352,7 +352,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
   p.pos = a.pos;
   p.heads = decode_heads(a.Hq / a.Hkv);
   p.hchunks = (a.Hq / a.Hkv + p.heads - 1) / p.heads;
-  p.splits = decode_splits(a.B, a.Hq, a.Hkv, a.num_sms);
+  p.splits = decode_splits(a.B, a.Hq, a.Hkv, a.num_sms, a.useful_splits);
   p.part_m = a.work;
   p.part_l = a.work + (size_t)a.B * a.Hq * p.splits;
   p.part_o = a.work + 2 * (size_t)a.B * a.Hq * p.splits;

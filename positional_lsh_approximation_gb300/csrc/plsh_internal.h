@@ -164,15 +164,26 @@ struct AttnArgs {
 // the union of their key envelopes; S is chosen for about three CTAs per SM
 // (at most 64).
 inline int decode_heads(int G) { return G < 8 ? G : 8; }
-inline int decode_splits(int B, int Hq, int Hkv, int num_sms) {
+// useful: shares worth having, from the widest envelope expected (at most 64)
+inline int decode_splits(int B, int Hq, int Hkv, int num_sms, int useful) {
   const int G = Hq / Hkv;
   const int64_t ctas = (int64_t)B * Hkv * ((G + decode_heads(G) - 1) / decode_heads(G));
   const int64_t want = 12LL * num_sms;
+  const int64_t cap = useful < 1 ? 1 : (useful > 64 ? 64 : useful);
   const int64_t sp = (want + ctas - 1) / ctas;
-  return (int)(sp < 1 ? 1 : (sp > 64 ? 64 : sp));
+  return (int)(sp < 1 ? 1 : (sp > cap ? cap : sp));
 }
-inline size_t decode_work_floats(int B, int Hq, int Hkv, int d, int num_sms) {
-  return (size_t)B * Hq * decode_splits(B, Hq, Hkv, num_sms) * (size_t)(d + 2);
+// the envelope of a row at pos under bins of scale sigma reaches about
+// 1.2 sigma keys back (the widest of the s bins around pos); a share of the
+// split takes about 64 keys of it
+inline int decode_useful_splits(double sigma_max, int pos) {
+  const double keys = 1.2 * sigma_max + 128.0;
+  const double lim = pos + 1.0 < keys ? pos + 1.0 : keys;
+  const double sp = lim / 64.0 + 1.0;
+  return sp > 64.0 ? 64 : (int)sp;
+}
+inline size_t decode_work_floats(int B, int Hq, int Hkv, int d, int num_sms, int useful) {
+  return (size_t)B * Hq * decode_splits(B, Hq, Hkv, num_sms, useful) * (size_t)(d + 2);
 }
 struct DecodeArgs {
   const void* q;         // [B, Hq, 1, d]
@@ -185,7 +196,8 @@ struct DecodeArgs {
   int pos;
   int dtype;             // PLSH_BF16 or PLSH_F32
   int num_sms;
-  float* work;           // decode_work_floats(B, Hq, Hkv, d, num_sms)
+  int useful_splits;     // decode_useful_splits of the widest bins
+  float* work;           // decode_work_floats(B, Hq, Hkv, d, num_sms, useful_splits)
   int* err;              // device error flag (bit 0: a bounded wait ran out)
   uint64_t wait_ns;
 };
