@@ -151,10 +151,11 @@ plsh_status plsh_bins_fixed(int64_t n, const int32_t* width_h, int32_t H, int32_
  * CUDA cores (every other case), fp32 accumulation, no atomics: a warp per
  * row computes the row's max, sum and sum_j P_ij dP_ij and dQ_i; a warp per
  * key then sums dK_j and dV_j over the rows whose bins contain it.
- * Scratch (3 B Hq n floats of row statistics, plus B Hq n d floats of dQ
- * accumulator on the tensor cores) lives in a device buffer the library
- * keeps per device between calls, grown on demand (which synchronises the
- * device); calls on different streams are ordered on it by an event.
+ * Scratch (2 or 3 B Hq n floats of row statistics, plus B Hq n d floats of
+ * dQ accumulator on the tensor cores) lives in a device buffer the library
+ * keeps per device between calls, grown on demand in stream order on
+ * `stream` (from the device's stream-ordered memory pool); calls on
+ * different streams are ordered on it by an event.
  * Asynchronous on `stream`.
  */
 plsh_status plsh_alibi_attn_backward(const plsh_tensor* Q, const plsh_tensor* K,
@@ -376,9 +377,10 @@ plsh_status plsh_alibi_exact(const plsh_tensor* Q, const plsh_tensor* K,
  * the union of their envelopes; the shares' partial results (max, row sum,
  * unnormalised P V) are merged into o.  The partials live in a device buffer
  * the library keeps per device (B * Hq * S * (d + 2) floats, S <= 64 shares
- * chosen so that about 12 CTAs per SM run; grown on demand, which
- * synchronises the device; calls on different streams are ordered on it by
- * an event).
+ * chosen so that about 12 CTAs per SM run, at most the 64-key shares of the
+ * envelope the widest bins are expected to reach; grown on demand in stream
+ * order on `stream`; calls on different streams are ordered on it by an
+ * event).
  * Asynchronous on `stream`; errors in the arguments return before any launch.
  */
 plsh_status plsh_alibi_decode(const plsh_tensor* q, const plsh_tensor* K,

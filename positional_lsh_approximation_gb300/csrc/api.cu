@@ -39,26 +39,35 @@ std::mutex g_ctx_mu;
 // held while a call enqueues work on a per-device scratch buffer
 std::mutex g_bwd_mu, g_decode_mu;
 
-plsh_status dev_alloc(void** p, size_t bytes, const char* what);
+bool fault_oom();
 
 // A per-device scratch buffer of at least `bytes`, ordered after its last
-// use on any stream: grown (after a device synchronisation, since earlier
-// calls may still read the old one) when too small; the calling stream
-// waits for the event recorded after the last use.  The caller holds the
-// buffer's mutex and records *ev on its stream after its launches.
+// use on any stream: the calling stream first waits for the event recorded
+// after that use; a buffer too small is then replaced in stream order on the
+// calling stream (freed, allocated from the device's stream-ordered pool and
+// zeroed there), so that growing it stalls neither the host nor other
+// streams.  The caller holds the buffer's mutex and records *ev on its stream
+// after its launches.
 plsh_status scratch_acquire(float** buf, size_t* have, cudaEvent_t* ev, size_t bytes,
                             cudaStream_t cs, const char* what) {
-  if (*have < bytes) {
-    PLSH_TRY_CUDA(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
-    cudaFree(*buf);
-    *buf = nullptr;
-    *have = 0;
-    plsh_status st = dev_alloc((void**)buf, bytes, what);
-    if (st != PLSH_OK) return st;
-    *have = bytes;
-  }
   if (*ev == nullptr) PLSH_TRY_CUDA(cudaEventCreateWithFlags(ev, cudaEventDisableTiming), what);
   PLSH_TRY_CUDA(cudaStreamWaitEvent(cs, *ev, 0), what);
+  if (*have < bytes) {
+    if (*buf != nullptr) PLSH_TRY_CUDA(cudaFreeAsync(*buf, cs), what);
+    *buf = nullptr;
+    *have = 0;
+    if (fault_oom()) return fail(PLSH_ERR_NOMEM, std::string(what) + ": injected allocation failure");
+    const cudaError_t e = cudaMallocAsync((void**)buf, bytes, cs);
+    if (e == cudaErrorMemoryAllocation) {
+      cudaGetLastError();
+      *buf = nullptr;
+      return fail(PLSH_ERR_NOMEM, std::string(what) + ": out of device memory");
+    }
+    PLSH_TRY_CUDA(e, what);
+    // zeroed once, so that counters kept in it start from a known state
+    PLSH_TRY_CUDA(cudaMemsetAsync(*buf, 0, bytes, cs), what);
+    *have = bytes;
+  }
   return PLSH_OK;
 }
 plsh::DeviceCtx g_ctx[kMaxDevices];
