@@ -247,15 +247,17 @@ void plsh_bins_free(plsh_bins* bins);
  *   Hq % Hkv == 0, bins->n == n, bins->H == Hq, d in {64, 128}.
  *   causal   non-zero: keys j <= i only.
  * Kernels (plsh_attn_path tells which one a call takes, without launching):
- *   tensor cores  bf16 with d = 128 and s within the kernel's shared memory
- *                 (s <= 47 causal, s <= 27 without the mask): QK^T in
+ *   tensor cores  bf16 with d in {64, 128} and s within the kernel's shared
+ *                 memory (s <= 47 causal, s <= 27 without the mask; d = 64
+ *                 runs zero-padded to 128 columns in shared memory, at the
+ *                 cost of d = 128): QK^T in
  *                 bf16, the weights P and V in f16 for P V (every bf16
  *                 value of V up to 65504 is an f16 value; P keeps 11
  *                 significant bits), fp32 accumulation and softmax.  A value of V beyond +-65504 is reported by
  *                 plsh_stream_status() as PLSH_ERR_RANGE (O is then not
  *                 valid); T~ is linear in V, so V scaled down by a power of
  *                 two gives O scaled down by the same power.
- *   CUDA cores    everything else (fp32, d = 64, larger s): fp32 throughout.
+ *   CUDA cores    everything else (fp32, larger s): fp32 throughout.
  * Asynchronous on `stream`.  A device-side wait that runs out (a bug, never
  * expected) is reported by the next plsh_stream_status().
  */
@@ -270,7 +272,8 @@ plsh_status plsh_alibi_attn(const plsh_tensor* Q, const plsh_tensor* K,
  * (so that T~_i = sum_j c_ij 2^{x_ij - lse_i} v_j), the statistic the backward
  * pass needs (plsh_alibi_attn_backward_lse).
  *   lse [B*Hq*n] fp32 device memory, row (b, h, i) at (b*Hq + h)*n + i.
- * Tensor-core path only (bf16, d = 128, s within its budget; plsh_attn_path):
+ * Tensor-core path only (bf16, d in {64, 128}, s within its budget;
+ * plsh_attn_path):
  * other inputs return PLSH_ERR_UNSUPPORTED.  O as for plsh_alibi_attn.
  * Asynchronous on `stream`.
  */

@@ -484,7 +484,7 @@ bool bwd_tc_ok(const plsh_tensor* Q, const plsh_tensor* K, const plsh_bins* bins
 // The tensor-core kernel serves bf16 with d = 128 and s within its shared
 // memory; everything else takes the CUDA-core kernel.
 bool tc_path_ok(int dtype, int64_t d, int s, int causal, int exact) {
-  return dtype == PLSH_BF16 && d == 128 &&
+  return dtype == PLSH_BF16 && (d == 128 || d == 64) &&
          plsh::attn_tc_smem_bytes(s, causal, exact) <= 232448;
 }
 
@@ -565,7 +565,7 @@ plsh_status run_attention(const plsh_tensor* Q, const plsh_tensor* K, const plsh
                                    : plsh::launch_attn_simt(a, slopes, Q->dtype, st);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   if (path == Path::Tc && tab.merges > 0) {
-    e = plsh::launch_split_merge(tab.merge, tab.merges, tab.ws, a.O, a.lse, a.Hq, a.n, st);
+    e = plsh::launch_split_merge(tab.merge, tab.merges, tab.ws, a.O, a.lse, a.Hq, a.n, a.d, st);
     if (e != cudaSuccess) return cuda_fail(e, "split merge launch");
   }
   return PLSH_OK;
@@ -1281,7 +1281,7 @@ plsh_status plsh_alibi_attn_noalloc(const plsh_tensor* Q, const plsh_tensor* K,
   if (bins->n != Q->n) return fail(PLSH_ERR_INVALID, "bins were drawn for another n");
   if (bins->H != Q->H) return fail(PLSH_ERR_INVALID, "bins were drawn for another number of heads");
   if ((st = check_bins_device(bins)) != PLSH_OK) return st;
-  if (!tc_path_ok(Q->dtype, Q->d, bins->s, causal ? 1 : 0, 0))
+  if (Q->d != 128 || !tc_path_ok(Q->dtype, Q->d, bins->s, causal ? 1 : 0, 0))
     return fail(PLSH_ERR_UNSUPPORTED, "allocation-free path: needs bf16, d = 128 and s within "
                                       "the tensor-core kernel's shared-memory budget");
   const int B = (int)Q->B, Hq = (int)Q->H, Hkv = (int)K->H;

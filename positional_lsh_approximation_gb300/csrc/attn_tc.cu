@@ -705,7 +705,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t s_col = tmem + lane_base + tile * BN;
     const uint32_t o_col = tmem + lane_base + kColO + tile * HD;
-    const float scale_log2 = 1.4426950408889634f * 0.08838834764831845f;  // log2(e)/sqrt(128)
+    // log2(e) / sqrt(d); d = 64 runs zero-padded to 128 columns
+    const float scale_log2 = 1.4426950408889634f * (a.d == 64 ? 0.125f : 0.08838834764831845f);
     const uint64_t scale2 = f2_pack(scale_log2, scale_log2);
     const int nlists = CAUSAL ? 1 : 2;
     int* bpl = bp + tile * nlists * s * BM;      // sorted bin starts, [s][BM]
@@ -796,7 +797,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         a.lse[row0 + i] = pend_l > 0.f ? pend_m + lg2(pend_l) : -INFINITY;
       }
 #pragma unroll 1
-      for (int q2 = 0; q2 < 2; ++q2) {
+      for (int q2 = 0; q2 < a.d / 64; ++q2) {          // d = 64: the padding's half is not stored
         uint32_t o0[32], o1[32];
         tmem_ld32(o_col + q2 * 64, o0);
         tmem_ld32(o_col + q2 * 64 + 32, o1);
@@ -817,7 +818,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                            pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
           } else if (qt >= 0 && i < n) {
             uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.O) +
-                                                   (row0 + i) * HD + q2 * 64);
+                                                   (row0 + i) * a.d + q2 * 64);
 #pragma unroll
             for (int v = 0; v < 4; ++v)
               orow[half * 4 + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
@@ -834,7 +835,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
             const uint4 v = ld_shared_v4(obuf + rr * 128 + ((c ^ (rr & 7)) << 4));
             const int ir = max(qt, 0) * BM + (warp & 3) * 32 + rr;
             if (qt >= 0 && ir < n)
-              reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.O) + (row0 + ir) * HD +
+              reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.O) + (row0 + ir) * a.d +
                                        q2 * 64)[c] = v;
           }
           __syncwarp();
@@ -1342,7 +1343,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
 // of the head dimension per lane.  Grid: (split items, 2 tiles, 16 row groups).
 __global__ void __launch_bounds__(256)
 split_merge_kernel(const int4* __restrict__ merge, const float* __restrict__ ws,
-                   __nv_bfloat16* __restrict__ O, float* __restrict__ lse, int Hq, int n) {
+                   __nv_bfloat16* __restrict__ O, float* __restrict__ lse, int Hq, int n, int d) {
   const int item = blockIdx.x, tile = blockIdx.y;
   const int r = blockIdx.z * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   const int4 e = merge[2 * item], x = merge[2 * item + 1];
@@ -1373,10 +1374,12 @@ split_merge_kernel(const int4* __restrict__ merge, const float* __restrict__ ws,
     o.w = fmaf(f, a4.w, o.w);
   }
   const float inv = l > 0.f ? 1.f / l : 0.f;
-  __nv_bfloat162* out =
-      reinterpret_cast<__nv_bfloat162*>(O + (((int64_t)e.x * Hq + h) * n + i) * HD) + 2 * lane;
-  out[0] = __floats2bfloat162_rn(o.x * inv, o.y * inv);
-  out[1] = __floats2bfloat162_rn(o.z * inv, o.w * inv);
+  if (4 * lane < d) {                                    // d = 64: the padding is not stored
+    __nv_bfloat162* out =
+        reinterpret_cast<__nv_bfloat162*>(O + (((int64_t)e.x * Hq + h) * n + i) * d) + 2 * lane;
+    out[0] = __floats2bfloat162_rn(o.x * inv, o.y * inv);
+    out[1] = __floats2bfloat162_rn(o.z * inv, o.w * inv);
+  }
   if (lse != nullptr && lane == 0)
     lse[((int64_t)e.x * Hq + h) * n + i] = l > 0.f ? m + __log2f(l) : -INFINITY;
 }
@@ -1403,13 +1406,16 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// [planes, n, 128] bf16 viewed as a 3-D tensor with 64 x 128 x 1 boxes and
-// 128-byte swizzle; rows past n read as zeros.
-bool make_map(CUtensorMap* map, const void* base, int64_t planes, int64_t n, int box_rows) {
+// [planes, n, d] bf16 (d = 64 or 128) viewed as a 3-D tensor with 64 x rows
+// x 1 boxes and 128-byte swizzle; rows past n, and with d = 64 the columns
+// past 64 (the second box of a tile), read as zeros, so that a d = 64 tile
+// enters the kernel zero-padded to 128 columns.
+bool make_map(CUtensorMap* map, const void* base, int64_t planes, int64_t n, int box_rows,
+              int d) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  const cuuint64_t dims[3] = {(cuuint64_t)HD, (cuuint64_t)n, (cuuint64_t)planes};
-  const cuuint64_t strides[2] = {(cuuint64_t)HD * 2, (cuuint64_t)n * HD * 2};
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)n, (cuuint64_t)planes};
+  const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)n * d * 2};
   const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
@@ -1472,7 +1478,7 @@ bool out_staged(int s, int causal, int exact) {
 }  // namespace
 
 bool make_tile_map_bf16(CUtensorMap* map, const void* base, int64_t planes, int64_t n) {
-  return make_map(map, base, planes, n, BM);
+  return make_map(map, base, planes, n, BM, HD);
 }
 
 size_t attn_tc_smem_bytes(int s, int causal, int exact) {
@@ -1480,19 +1486,19 @@ size_t attn_tc_smem_bytes(int s, int causal, int exact) {
 }
 
 cudaError_t launch_split_merge(const int4* merge, int count, const float* ws, void* O, float* lse,
-                               int Hq, int n, cudaStream_t st) {
+                               int Hq, int n, int d, cudaStream_t st) {
   if (count <= 0) return cudaSuccess;
   split_merge_kernel<<<dim3((unsigned)count, 2, BM / 8), 256, 0, st>>>(
-      merge, ws, static_cast<__nv_bfloat16*>(O), lse, Hq, n);
+      merge, ws, static_cast<__nv_bfloat16*>(O), lse, Hq, n, d);
   return cudaGetLastError();
 }
 
 cudaError_t launch_attn_tc(const AttnArgs& a, const float* slopes_host,
                            int num_sms, cudaStream_t st) {
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, a.Q, (int64_t)a.B * a.Hq, a.n, BM) ||
-      !make_map(&mk, a.K, (int64_t)a.B * a.Hkv, a.n, BN) ||
-      !make_map(&mv, a.V, (int64_t)a.B * a.Hkv, a.n, BN))
+  if (!make_map(&mq, a.Q, (int64_t)a.B * a.Hq, a.n, BM, a.d) ||
+      !make_map(&mk, a.K, (int64_t)a.B * a.Hkv, a.n, BN, a.d) ||
+      !make_map(&mv, a.V, (int64_t)a.B * a.Hkv, a.n, BN, a.d))
     return cudaErrorInvalidValue;
   TcParams p;
   p.a = a;

@@ -213,7 +213,7 @@ cudaError_t launch_attn_tc(const AttnArgs& a, const float* slopes_host,
 // combines the parts of `count` split items (entries of `merge`, two int4
 // each) into O (bf16 [B, Hq, n, 128])
 cudaError_t launch_split_merge(const int4* merge, int count, const float* ws, void* O, float* lse,
-                               int Hq, int n, cudaStream_t st);
+                               int Hq, int n, int d, cudaStream_t st);
 size_t attn_tc_smem_bytes(int s, int causal, int exact);
 // [planes, n, 128] bf16 as a TMA tensor map with 64 x 128 x 1 boxes, 128-byte
 // swizzle, rows past n reading as zeros (attn_tc.cu)

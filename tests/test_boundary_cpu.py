@@ -168,7 +168,7 @@ def test_attn_path_query(lib):
         return out.value
 
     assert path(plsh.PLSH_BF16, 128) == plsh.PLSH_PATH_TENSOR_CORES      # exact ALiBi
-    assert path(plsh.PLSH_BF16, 64) == plsh.PLSH_PATH_CUDA_CORES
+    assert path(plsh.PLSH_BF16, 64) == plsh.PLSH_PATH_TENSOR_CORES      # zero-padded to 128
     assert path(plsh.PLSH_F32, 128) == plsh.PLSH_PATH_CUDA_CORES
     assert lib.plsh_attn_path(None, None, 1, ctypes.byref(out)) == plsh.PLSH_ERR_INVALID
 

@@ -108,6 +108,10 @@ SMALL = [
     ("bf16_causal_ragged", 1, 4, 2, 1000, 128, "bf16", True, 10, (1.2, 6.0, 40.0, 300.0)),
     ("bf16_noncausal_ragged", 2, 2, 1, 777, 128, "bf16", False, 6, (3.0, 150.0)),
     ("bf16_d64", 1, 2, 1, 513, 64, "bf16", True, 4, (5.0, 60.0)),
+    # d = 64 on the tensor cores (zero-padded to 128 columns): GQA, without
+    # the mask, ragged tails
+    ("bf16_d64_gqa_s10", 1, 4, 2, 700, 64, "bf16", True, 10, (1.2, 6.0, 40.0, 300.0)),
+    ("bf16_d64_noncausal", 2, 2, 1, 390, 64, "bf16", False, 6, (3.0, 150.0)),
     ("bf16_s24", 1, 2, 1, 700, 128, "bf16", True, 24, (3.0, 50.0)),
     ("bf16_s48", 1, 2, 2, 640, 128, "bf16", True, 48, (2.0, 30.0)),
     ("bf16_s64", 1, 2, 2, 640, 128, "bf16", True, 64, (2.0, 30.0)),
@@ -344,6 +348,7 @@ SPLIT_CASES = [
     ("noncausal", 2, 2, 1, 777, 128, False, 6, (3.0, 150.0)),
     ("odd_group", 1, 3, 1, 900, 128, True, 7, (2.5, 90.0, 400.0)),
     ("sorted_lists", 1, 2, 1, 700, 128, True, 24, (3.0, 50.0)),
+    ("d64", 1, 2, 1, 800, 64, True, 8, (40.0, 600.0)),
 ]
 
 
