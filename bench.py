@@ -384,7 +384,7 @@ def run_ours(args, rank, world):
 
 # ------------------------------------------------ the other workloads
 CONFIG_NAMES = ["qwen_s10", "qwen_s20", "sweep_s1", "sweep_s5", "sweep_s10", "sweep_s20",
-                "sweep_s40", "scout"]
+                "sweep_s40", "scout", "mistral_d64"]
 
 
 def device_qkv(w, seed):

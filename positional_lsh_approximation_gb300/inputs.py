@@ -65,6 +65,9 @@ WORKLOADS = {
     # one attention layer of a Mistral-7B-shaped model (GQA 32/8)
     "mistral": Workload("mistral", 1, 32, 8, 8192, 128, "bf16", True, 10,
                         qkv_seed=1001),
+    # the same layer with 64-wide heads (tensor cores, zero-padded to 128)
+    "mistral_d64": Workload("mistral_d64", 1, 32, 8, 8192, 64, "bf16", True, 10,
+                            qkv_seed=1005),
     # Qwen3-0.6B-shaped layer, 5% of token rows of Q and K scaled by 8
     "qwen_s10": Workload("qwen_s10", 4, 16, 8, 8192, 128, "bf16", True, 10,
                          peaky_frac=0.05, qkv_seed=1002),
