@@ -28,22 +28,26 @@
 // Q is double buffered, so the next step's S^T runs while this step's dQ_p
 // is being drained; the next dP^T waits for that drain.
 //
-// One thread per key turns a row of S^T, dP^T into P^T, dS^T (bf16).  Its
-// multiplicities over a chunk of 32 query rows are a running count: the
-// hashes whose bin around the key is open at the chunk's first row, minus a
-// step at each bin end inside the chunk (plus a step at each bin start when
-// not causal), one bit per row; rows past every bin end or before every start
-// are masked.  Chunks that every bin of every key of the warp spans take
-// c = s, folded into the exponent.  The same threads stage each step's dQ_p
-// rows in shared memory, where TMA reductions add them to an fp32
-// accumulator in global memory (several key tiles reach a query row), and,
-// at the end of an item, write dK and dV of their key.
+// Two threads per key (warps w and w + 4 share a TMEM lane quarter, each
+// taking half of the step's query columns) turn a row of S^T, dP^T into P^T,
+// dS^T (bf16).  A key's multiplicities over a chunk of 32 query rows are a
+// running count: the hashes whose bin around the key is open at the chunk's
+// first row, minus the bins that end at each row inside the chunk (plus
+// those that start there when not causal), held as binary planes; rows past
+// every bin end or before every start are masked.  Chunks that every bin of
+// every key of the warp spans take c = s, folded into the exponent.  The bins
+// sit in a compile-time number of register slots (SREG >= s).  The same
+// threads stage each step's dQ_p rows in shared memory, where TMA reductions
+// add them to an fp32 accumulator in global memory (several key tiles reach
+// a query row), and, at the end of an item, write their half of dK and dV of
+// their key.
 //
-// Warps: 0-3 compute (thread = TMEM lane), 4 producer (item queue, query-tile
-// ranges from the bin records, TMA of K, V per item and of Q, dO plus the
-// rows' statistics per step, L2 prefetch of the next step's), 5 one thread
-// issuing tcgen05.mma.  Items are taken in the order of their KV group's
-// expected work, largest first.
+// Warps: 0-7 compute (thread = TMEM lane, two warps per lane quarter), 8
+// producer (item queue, query-tile ranges from the bin records, TMA of K, V
+// per item and of Q, dO per step, the rows' statistics and the head's bin
+// records per step into shared memory, L2 prefetch of the next step's
+// tiles), 9 one thread issuing tcgen05.mma.  Items are taken in the order of
+// their KV group's expected work, largest first.
 // Every mbarrier wait is bounded; on expiry the CTA raises the error flag,
 // lets its copies and MMAs drain, frees TMEM and exits.
 #include <cuda.h>
