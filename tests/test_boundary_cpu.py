@@ -176,3 +176,27 @@ def test_attn_path_query(lib):
 def test_split_parts_setting_is_validated(lib):
     assert lib.plsh_set_split_parts(-1) == plsh.PLSH_ERR_INVALID
     assert lib.plsh_set_split_parts(17) == plsh.PLSH_ERR_INVALID
+
+
+def test_log_sum_exp_entry_points_reject_bad_arguments(lib):
+    """The forward with log-sum-exp and the backward from saved statistics
+    validate before any launch: a missing lse or O, an O of another shape."""
+    T = plsh._Tensor
+    q = T(256, plsh.PLSH_BF16, 1, 2, 128, 128)
+    k = T(256, plsh.PLSH_BF16, 1, 1, 128, 128)
+    o = T(256, plsh.PLSH_BF16, 1, 2, 128, 128)
+    lse = ctypes.c_void_p(4096)
+    st = lib.plsh_alibi_attn_lse(ctypes.byref(q), ctypes.byref(k), ctypes.byref(k), None, 1,
+                                 ctypes.byref(o), None, None)
+    assert st == plsh.PLSH_ERR_INVALID                     # lse NULL
+    st = lib.plsh_alibi_attn_lse(ctypes.byref(q), ctypes.byref(k), ctypes.byref(k), None, 1,
+                                 ctypes.byref(o), lse, None)
+    assert st == plsh.PLSH_ERR_INVALID                     # bins NULL
+
+    def bwd(o_, lse_):
+        return lib.plsh_alibi_attn_backward_lse(
+            ctypes.byref(q), ctypes.byref(k), ctypes.byref(k), o_, lse_, ctypes.byref(q), None, 1,
+            ctypes.byref(q), ctypes.byref(k), ctypes.byref(k), None)
+    assert bwd(None, lse) == plsh.PLSH_ERR_INVALID          # O NULL
+    assert bwd(ctypes.byref(T(256, plsh.PLSH_BF16, 1, 2, 64, 128)), lse) == plsh.PLSH_ERR_INVALID
+    assert bwd(ctypes.byref(o), None) == plsh.PLSH_ERR_INVALID   # lse NULL
