@@ -11,9 +11,13 @@
 //   bin starts: 0 and ceil(u + k w), k = 0, 1, ... below n, u + k w one
 //   fused multiply-add (all positions when w < 1).
 // All fp64 arithmetic is done one correctly rounded operation at a time
-// (__dadd_rn, __fma_rn etc.), with the library's own logarithm, so the
-// boundaries are reproducible bit for bit by any implementation of the same
-// recipe.
+// (__dadd_rn, __fma_rn etc.), with a logarithm of its own built from such
+// operations, so the boundaries are reproducible bit for bit by any
+// implementation of the same recipe.  Steps that are exact in any case (an
+// integer to double, a double's ceiling, scaling by a power of two, the
+// comparison of two doubles of one binade) are done on the bits with integer
+// instructions: this part issues fp64 instructions, conversions included, at
+// a small fraction of its integer rate and with a long latency.
 //
 // Output layout: for every hash, one BinRecord per 32 positions (bitmap of
 // bin starts plus the neighbouring starts), which the attention kernels read
@@ -52,6 +56,39 @@ __device__ __forceinline__ void philox4x32_10(uint32_t c[4], uint32_t k0,
   }
 }
 
+// Bits of a double as an unsigned integer and back.
+__device__ __forceinline__ uint64_t dbits(double x) {
+  return (uint64_t)__double_as_longlong(x);
+}
+__device__ __forceinline__ double dfrom(uint64_t b) { return __longlong_as_double((long long)b); }
+
+// (double)k for 0 <= k < 2^53, exactly: the leading one sets the exponent.
+__device__ __forceinline__ double ll_to_double(uint64_t k) {
+  if (k == 0) return 0.0;
+  const int e = 63 - __clzll((long long)k);    // 2^e <= k < 2^(e+1)
+  return dfrom(((uint64_t)(1023 + e) << 52) | ((k << (52 - e)) & 0x000fffffffffffffull));
+}
+
+// ceil(r) for 0 <= r < 2^62, exactly: the integer part of the significand,
+// plus one when a fraction bit is set.
+__device__ __forceinline__ long long ceil_to_ll(double r) {
+  const uint64_t b = dbits(r);
+  const int ex = (int)(b >> 52) - 1023;        // r = 1.f 2^ex
+  if (ex < 0) return b == 0 ? 0 : 1;
+  const uint64_t m = (b & 0x000fffffffffffffull) | (1ull << 52);
+  if (ex >= 52) return (long long)(m << (ex - 52));
+  const int fr = 52 - ex;
+  return (long long)((m >> fr) + ((m & ((1ull << fr) - 1ull)) != 0ull));
+}
+
+// A positive normal double within float's normal range as a float,
+// truncated (error below 2^-23 relative).
+__device__ __forceinline__ float to_float_rz(double x) {
+  const uint64_t b = dbits(x);
+  const uint32_t e = (uint32_t)((b >> 52) & 0x7ff) - 1023u + 127u;
+  return __uint_as_float((e << 23) | (uint32_t)((b >> 29) & 0x7fffffu));
+}
+
 // Natural log of a positive normal double: x = 2^e m, m reduced to
 // [sqrt(1/2), sqrt(2)), ln m = 2 atanh(z) = 2 z sum_k z^2k / (2k+1) with
 // z = (m-1)/(m+1), 12 terms by Horner with fused multiply-adds, then e ln2
@@ -65,8 +102,10 @@ __device__ double ln_rn(double x) {
   long long e = ((bits >> 52) & 0x7ff) - 1023;
   double m = __longlong_as_double((bits & 0x000fffffffffffffll) |
                                   0x3ff0000000000000ll);
-  if (m > kSqrt2) {
-    m = __dmul_rn(m, 0.5);
+  // m and sqrt(2) share a binade, so they compare as integers; halving m
+  // lowers its exponent by one
+  if (dbits(m) > dbits(kSqrt2)) {
+    m = dfrom(dbits(m) - (1ull << 52));
     e += 1;
   }
   // 1/(2k+1), each the correctly rounded quotient (folded by the compiler)
@@ -84,9 +123,10 @@ __device__ double ln_rn(double x) {
                    __fma_rn(ed, kLn2Lo, ln_m));
 }
 
-// ceil(u + k w) with the multiply and the add rounded separately.
+// ceil(u + k w), the multiply-add rounded once (0 <= k < 2^53, 0 < u + k w
+// < 2^62).
 __device__ __forceinline__ long long start_of(long long k, double w, double u) {
-  return __double2ll_ru(__fma_rn((double)k, w, u));   // ceil(u + k w), rounded once
+  return ceil_to_ll(__fma_rn(ll_to_double((uint64_t)k), w, u));
 }
 
 // One thread per listed start (terminal entries excluded): set its bit.
@@ -235,10 +275,13 @@ sample_kernel(int64_t n, int64_t W, int nseg, int spc, int s,
     const int h = hs / s, t = hs % s;
     uint32_t c[4] = {(uint32_t)t, (uint32_t)h, 0u, 0u};
     philox4x32_10(c, (uint32_t)(seed & 0xffffffffu), (uint32_t)(seed >> 32));
-    const double two_m32 = 0x1p-32;
-    const double uk = __dmul_rn(__dadd_rn((double)c[threadIdx.x], 0.5), two_m32);
-    lnv[threadIdx.x] = ln_rn(uk);
-    if (threadIdx.x == 0) wu[1] = __dmul_rn(__dadd_rn((double)c[2], 0.5), two_m32);
+    // U = (x + 0.5) 2^-32 = (2x + 1) 2^-33, exact: the odd integer 2x + 1 as
+    // a double, its exponent lowered by 33
+    auto unit = [](uint32_t x) {
+      return dfrom(dbits(ll_to_double(2ull * x + 1ull)) - (33ull << 52));
+    };
+    lnv[threadIdx.x] = ln_rn(unit(c[threadIdx.x]));
+    if (threadIdx.x == 0) wu[1] = unit(c[2]);
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -253,6 +296,7 @@ sample_kernel(int64_t n, int64_t W, int nseg, int spc, int s,
   }
   __syncthreads();
   const double w = wu[0], u = wu[1];
+  const bool wide = dbits(w) >= dbits(1.0);    // w >= 1 (w > 0)
   for (int sg = sg0; sg < min(nseg, sg0 + spc); ++sg) {
     const int64_t seg = (int64_t)sg * kSegWords;
     const int nw = (int)min((int64_t)kSegWords, W - seg);
@@ -265,8 +309,8 @@ sample_kernel(int64_t n, int64_t W, int nseg, int spc, int s,
       // k range of the walk, from just below the first start that can reach
       // the segment to just past the first start at or beyond P1; estimated
       // in fp32 (no fp64 division) with a slack that covers its rounding
-      if (w >= 1.0) {
-        const float wf = (float)w, uf = (float)u;
+      if (wide) {
+        const float wf = to_float_rz(w), uf = to_float_rz(u);
         const float ka = ((float)(P0 - 1) - uf) / wf;
         const float kb = ((float)P1 - uf) / wf;
         const float slack = 2.0f + fmaxf(fabsf(ka), fabsf(kb)) * 0x1p-18f;
@@ -276,7 +320,7 @@ sample_kernel(int64_t n, int64_t W, int nseg, int spc, int s,
       }
     }
     __syncthreads();
-    if (w < 1.0) {   // every position opens a bin
+    if (!wide) {     // w < 1: every position opens a bin
       if (threadIdx.x < nw) {
         const int64_t lo = P0 + (int64_t)threadIdx.x * 32;
         const int64_t cnt = min((int64_t)32, P1 - lo);
