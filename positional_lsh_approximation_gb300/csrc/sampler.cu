@@ -222,8 +222,8 @@ prev_next_kernel(int64_t n, int64_t W, BinRecord* __restrict__ rec) {
 // the segment's bin starts set in a shared-memory bitmap (one thread per k,
 // start ceil(u + k w)), the last start before the segment and the first after
 // it taken from the same k walk, and the records from two block scans.
-constexpr int kSampThreads = 128;
-constexpr int kSegWords = 64;
+constexpr int kSampThreads = 256;
+constexpr int kSegWords = 128;
 
 // Block-wide exclusive scan of `v` with operator max (fwd) or min (!fwd):
 // thread t receives the combination of threads before it (after it for !fwd)
@@ -375,10 +375,10 @@ sample_kernel(int64_t n, int64_t W, int nseg, int spc, int s,
 
 cudaError_t launch_sample(plsh_bins* b, uint64_t seed, cudaStream_t st) {
   const int HS = b->H * b->s;
-  // about 2048 CTAs whatever the shape: each takes spc consecutive segments
+  // about 1024 CTAs whatever the shape: each takes spc consecutive segments
   // of one hash and computes that hash's draw once
   const int64_t nseg = (b->W + kSegWords - 1) / kSegWords;
-  const int64_t target = 2048;
+  const int64_t target = 1024;
   const int64_t spc = std::max<int64_t>(1, (HS * nseg + target - 1) / target);
   const int64_t cps = (nseg + spc - 1) / spc;
   sample_kernel<<<(unsigned)(HS * cps), kSampThreads, 0, st>>>(
