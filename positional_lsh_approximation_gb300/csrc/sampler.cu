@@ -308,15 +308,18 @@ sample_kernel(int64_t n, int64_t W, int nseg, int spc, int s,
       prev_s = P0 > 0 ? 0 : -1;    // position 0 always opens a bin
       // k range of the walk, from just below the first start that can reach
       // the segment to just past the first start at or beyond P1; estimated
-      // in fp32 (no fp64 division) with a slack that covers its rounding
+      // in fp32 (no fp64 division; a fast reciprocal, positions as int32 and
+      // k as uint32, so that no conversion takes the fp64 pipe) with a slack
+      // that covers its rounding (relative error below 2^-20)
       if (wide) {
         const float wf = to_float_rz(w), uf = to_float_rz(u);
-        const float ka = ((float)(P0 - 1) - uf) / wf;
-        const float kb = ((float)P1 - uf) / wf;
+        const float rw = __fdividef(1.0f, wf);
+        const float ka = ((float)(int32_t)(P0 - 1) - uf) * rw;
+        const float kb = ((float)(int32_t)P1 - uf) * rw;
         const float slack = 2.0f + fmaxf(fabsf(ka), fabsf(kb)) * 0x1p-18f;
-        const float lo = floorf(ka - slack), hi = ceilf(kb + slack);
-        k0_s = lo > 0.0f ? (long long)lo : 0ll;
-        k1_s = hi > 0.0f ? (long long)hi : 0ll;
+        const float lo = floorf(ka - slack), hi = fminf(ceilf(kb + slack), 4294967040.0f);
+        k0_s = lo > 0.0f ? (long long)(uint32_t)lo : 0ll;
+        k1_s = hi > 0.0f ? (long long)(uint32_t)hi : 0ll;
       }
     }
     __syncthreads();
