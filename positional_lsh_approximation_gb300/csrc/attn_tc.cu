@@ -330,6 +330,23 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       // pop until an item with work (a split item's part past its key
       // envelope only marks its rows empty) or the end of the queue
       bool published = false, drained = false;
+      if (seq >= 2 && a.item_ext != nullptr) {
+        // with split items (long envelopes, few items) at most one item
+        // waits behind the one in progress near the end of the queue: three
+        // long items held per CTA while others run dry leave a long tail
+        // (with short items the deeper lookahead pays more than the tail
+        // costs)
+        int head = 0;
+        if (lane == 0) head = *reinterpret_cast<volatile int*>(a.queue);
+        head = __shfl_sync(FULL, head, 0);
+        if (a.num_items - head < kRing * (int)gridDim.x) {
+          const int j = seq - 2;
+          if (lane == 0)
+            ok = mbar_wait(bar(B_IEMPTY + j % kRing), (uint32_t)(j / kRing) & 1u, abort, lim);
+          ok = __shfl_sync(FULL, (int)ok, 0) != 0;
+          if (!ok) break;
+        }
+      }
       while (!published) {
       int idx = 0;
       if (lane == 0) idx = atomicAdd(a.queue, 1);
