@@ -330,12 +330,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       // pop until an item with work (a split item's part past its key
       // envelope only marks its rows empty) or the end of the queue
       bool published = false, drained = false;
-      if (seq >= 2 && a.item_ext != nullptr) {
-        // with split items (long envelopes, few items) at most one item
-        // waits behind the one in progress near the end of the queue: three
-        // long items held per CTA while others run dry leave a long tail
-        // (with short items the deeper lookahead pays more than the tail
-        // costs)
+      if (seq >= 2) {
+        // near the end of the queue at most one item waits behind the one in
+        // progress: three items held per CTA while others run dry left the
+        // last CTA up to two items behind the rest (a shallower lookahead
+        // cannot be had: the MMA thread sees the next item published before
+        // it issues an item's last P V, which the release of that item needs)
         int head = 0;
         if (lane == 0) head = *reinterpret_cast<volatile int*>(a.queue);
         head = __shfl_sync(FULL, head, 0);
