@@ -288,7 +288,9 @@ struct ItemList {
 // head.  Heads of a KV group pair up (sorted by sigma so that paired heads
 // have similar key envelopes); an odd group's last head pairs its own row
 // tiles.  Ordered by expected cost, largest first, so that the dynamic queue
-// balances like longest-processing-time scheduling.
+// balances like longest-processing-time scheduling: the key tiles the item
+// is expected to run (the diagonal tile plus the look-back of its heads'
+// widest bins, clipped at the sequence start), then sigma and row tile.
 //
 // Key-range split: with split_parts = 0 an item whose expected key tiles
 // exceed half the per-SM share of the whole call (at least 2) is cut into
@@ -346,8 +348,13 @@ ItemList build_items(int B, int Hq, int Hkv, int QT, int qt0, int qt1, bool exac
   }
   std::vector<size_t> order(items.size());
   std::iota(order.begin(), order.end(), 0);
-  std::stable_sort(order.begin(), order.end(),
-                   [&](size_t x, size_t y) { return cost[x] > cost[y]; });
+  // longest first by the expected key tiles of a part, then by sigma and
+  // row tile
+  std::stable_sort(order.begin(), order.end(), [&](size_t x, size_t y) {
+    const double tx = tiles[x] / parts[x], ty = tiles[y] / parts[y];
+    if (tx != ty) return tx > ty;
+    return cost[x] > cost[y];
+  });
   ItemList out;
   bool any_split = false;
   for (int pc : parts) any_split = any_split || pc > 1;
