@@ -80,7 +80,7 @@ constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kSchedWarp = 10;
 constexpr int kConvWarp = 11;
-constexpr int kRing = 3;                         // work items in flight
+constexpr int kRing = 2;                         // work items in flight
 constexpr int kSlots = 3;                        // K/V tile ring depth
 constexpr int kMaxSlots = 4;                     // barriers reserved for the ring
 constexpr uint32_t kTileBytes = BM * HD * 2;     // 32 KB bf16 tile
@@ -319,7 +319,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
   if (warp == kSchedWarp) {
     // ----------------------------------------------------------- scheduler
     // pops items, stages the rows' bin records, finds the key envelope and
-    // publishes the item up to kRing - 1 items ahead of its consumers
+    // publishes the item up to kRing - 1 items ahead of its consumers: one
+    // item waits behind the one in progress (the least the MMA thread
+    // allows: it sees the next item published before it issues an item's
+    // last P V).  A deeper lookahead (two items) left the last CTA up to two
+    // items behind the rest when the queue ran dry and was no faster before
     bool ok = true;
     for (int seq = 0; !a.stall; ++seq) {   // stall: fault injection
       const int slot = seq % kRing;
@@ -330,23 +334,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       // pop until an item with work (a split item's part past its key
       // envelope only marks its rows empty) or the end of the queue
       bool published = false, drained = false;
-      if (seq >= 2) {
-        // near the end of the queue at most one item waits behind the one in
-        // progress: three items held per CTA while others run dry left the
-        // last CTA up to two items behind the rest (a shallower lookahead
-        // cannot be had: the MMA thread sees the next item published before
-        // it issues an item's last P V, which the release of that item needs)
-        int head = 0;
-        if (lane == 0) head = *reinterpret_cast<volatile int*>(a.queue);
-        head = __shfl_sync(FULL, head, 0);
-        if (a.num_items - head < kRing * (int)gridDim.x) {
-          const int j = seq - 2;
-          if (lane == 0)
-            ok = mbar_wait(bar(B_IEMPTY + j % kRing), (uint32_t)(j / kRing) & 1u, abort, lim);
-          ok = __shfl_sync(FULL, (int)ok, 0) != 0;
-          if (!ok) break;
-        }
-      }
       while (!published) {
       int idx = 0;
       if (lane == 0) idx = atomicAdd(a.queue, 1);
