@@ -248,7 +248,7 @@ void plsh_bins_free(plsh_bins* bins);
  *   causal   non-zero: keys j <= i only.
  * Kernels (plsh_attn_path tells which one a call takes, without launching):
  *   tensor cores  bf16 with d in {64, 128} and s within the kernel's shared
- *                 memory (s <= 47 causal, s <= 27 without the mask; d = 64
+ *                 memory (s <= 52 causal, s <= 29 without the mask; d = 64
  *                 runs zero-padded to 128 columns in shared memory, at the
  *                 cost of d = 128): QK^T in
  *                 bf16, the weights P and V in f16 for P V (every bf16
@@ -259,7 +259,12 @@ void plsh_bins_free(plsh_bins* bins);
  *                 two gives O scaled down by the same power.
  *   CUDA cores    everything else (fp32, larger s): fp32 throughout.
  * Asynchronous on `stream`.  A device-side wait that runs out (a bug, never
- * expected) is reported by the next plsh_stream_status().
+ * expected) is reported by the next plsh_stream_status().  The tensor-core
+ * path keeps a work-item table per shape and head order on the device
+ * (allocated and uploaded on `stream` at the first call of a shape, in stream
+ * order; up to 16 are cached, and the least recently used one that no call
+ * holds is freed, in stream order behind the work of the calls that used
+ * it, when a seventeenth shape arrives).
  */
 plsh_status plsh_alibi_attn(const plsh_tensor* Q, const plsh_tensor* K,
                             const plsh_tensor* V, const plsh_bins* bins,
@@ -297,7 +302,7 @@ plsh_status plsh_alibi_attn_lse(const plsh_tensor* Q, const plsh_tensor* K,
  * allocation routine.
  *
  * Limits: bf16, d = 128, s within the tensor-core kernel's shared-memory
- * budget (s <= 47 causal, s <= 27 without the mask), at most 1023 query
+ * budget (s <= 52 causal, s <= 29 without the mask), at most 1023 query
  * heads and 65536 work items (one item per two 128-row query tiles:
  * B * Hq * ceil(n/128) / 2, e.g.
  * n = 131072 with 40 heads uses 20480); larger requests return
@@ -338,10 +343,11 @@ plsh_status plsh_noalloc_status(void* stream);
  * are host pointers (page-locked memory lets the copies run asynchronously
  * and overlap; pageable memory works but each copy then blocks the calling
  * thread).  The library stages the tensors through device buffers it keeps
- * per device (grown on demand, which synchronises the device; held until the
- * process exits) and splits the query rows into up to four chunks on the
- * tensor-core path: chunk c + 1 is copied in and chunk c - 1 copied out, on
- * two copy streams of its own, while the fused kernel runs on chunk c (with
+ * per device (grown on demand in stream order, behind the previous call of
+ * this entry point; held until the process exits) and splits the query rows
+ * into up to four chunks on the tensor-core path: chunk c + 1 is copied in
+ * and chunk c - 1 copied out, on two copy streams of its own, while the
+ * fused kernel runs on chunk c (with
  * the causal mask only the keys up to a chunk's last row are needed before
  * it starts).  The call returns once everything is queued; O is complete on
  * the host when `stream` reaches the point of the call (synchronise it before

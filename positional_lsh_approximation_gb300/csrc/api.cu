@@ -93,6 +93,21 @@ plsh_status dev_alloc(void** p, size_t bytes, const char* what) {
   return PLSH_OK;
 }
 
+// The same, ordered on `st` (no implicit synchronisation; free with
+// cudaFreeAsync).
+plsh_status dev_alloc_async(void** p, size_t bytes, cudaStream_t st, const char* what) {
+  *p = nullptr;
+  if (fault_oom()) return fail(PLSH_ERR_NOMEM, std::string(what) + ": injected allocation failure");
+  cudaError_t e = cudaMallocAsync(p, bytes == 0 ? 16 : bytes, st);
+  if (e == cudaErrorMemoryAllocation) {
+    cudaGetLastError();
+    *p = nullptr;
+    return fail(PLSH_ERR_NOMEM, std::string(what) + ": out of device memory");
+  }
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  return PLSH_OK;
+}
+
 // Context of the current device, created on first use.
 plsh_status current_ctx(plsh::DeviceCtx** out) {
   int dev = -1;
@@ -385,14 +400,67 @@ struct TableRef {
   const int4* merge = nullptr;
   int merges = 0;
   float* ws = nullptr;
+  plsh::ItemTable* table = nullptr;   // pinned until table_release
 };
 
-void free_table(plsh::ItemTable& t) {
-  cudaFree(t.dev);
-  cudaFree(t.dev_ext);
-  cudaFree(t.dev_merge);
-  cudaFree(t.ws);
+// Frees a table's device memory on `st` once the work of every call that
+// used it is done (stream-ordered: the host does not wait).
+void free_table(plsh::ItemTable& t, cudaStream_t st) {
+  for (auto& u : t.uses) {
+    cudaStreamWaitEvent(st, u.second, 0);
+    cudaEventDestroy(u.second);
+  }
+  t.uses.clear();
+  if (t.ready != nullptr) {
+    cudaStreamWaitEvent(st, t.ready, 0);
+    cudaEventDestroy(t.ready);
+    t.ready = nullptr;
+  }
+  for (void* q : {(void*)t.dev, (void*)t.dev_ext, (void*)t.dev_merge, (void*)t.ws})
+    if (q != nullptr) cudaFreeAsync(q, st);
+  t.dev = nullptr;
+  t.dev_ext = nullptr;
+  t.dev_merge = nullptr;
+  t.ws = nullptr;
 }
+
+// Ends a call's hold on its table: an event behind the call's work on `st`
+// (one per stream that used the table; beyond eight streams the oldest
+// entry is taken over once its work is done) and the pin released.
+void table_release(TableRef& tab, cudaStream_t st, bool used) {
+  if (tab.table == nullptr) return;
+  std::lock_guard<std::mutex> lk(g_ctx_mu);
+  plsh::ItemTable& t = *tab.table;
+  if (used) {
+    cudaEvent_t ev = nullptr;
+    for (auto& u : t.uses)
+      if (u.first == st) ev = u.second;
+    if (ev == nullptr) {
+      if (t.uses.size() >= 8) {
+        cudaEventSynchronize(t.uses.front().second);
+        ev = t.uses.front().second;
+        t.uses.erase(t.uses.begin());
+      } else if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) {
+        ev = nullptr;
+      }
+      if (ev != nullptr) t.uses.emplace_back(st, ev);
+    }
+    if (ev == nullptr || cudaEventRecord(ev, st) != cudaSuccess) {
+      // no event to order the free behind: keep the table from eviction
+      t.pins += 1;
+    }
+  }
+  t.pins -= 1;
+  tab.table = nullptr;
+}
+
+// Releases a call's table hold on every path out of the call.
+struct TableHold {
+  TableRef* tab;
+  cudaStream_t st;
+  bool used = false;
+  ~TableHold() { table_release(*tab, st, used); }
+};
 
 plsh_status item_table(plsh::DeviceCtx* ctx, int B, int Hq, int Hkv, int QT, int qt0, int qt1,
                        bool exact, bool causal, int s, const std::vector<double>& sigma,
@@ -424,12 +492,17 @@ plsh_status item_table(plsh::DeviceCtx* ctx, int B, int Hq, int Hkv, int QT, int
   auto it = ctx->tables.find(key);
   if (it == ctx->tables.end()) {
     if (ctx->tables.size() >= plsh::kMaxTables) {
-      auto victim = ctx->tables.begin();
+      // the least recently used table that no call holds, freed behind the
+      // work that used it (if every table is held, the cache grows instead)
+      auto victim = ctx->tables.end();
       for (auto jt = ctx->tables.begin(); jt != ctx->tables.end(); ++jt)
-        if (jt->second.last_use < victim->second.last_use) victim = jt;
-      cudaDeviceSynchronize();
-      free_table(victim->second);
-      ctx->tables.erase(victim);
+        if (jt->second.pins == 0 &&
+            (victim == ctx->tables.end() || jt->second.last_use < victim->second.last_use))
+          victim = jt;
+      if (victim != ctx->tables.end()) {
+        free_table(victim->second, st);
+        ctx->tables.erase(victim);
+      }
     }
     plsh::ItemTable t;
     ItemList lst = build_items(B, Hq, Hkv, QT, qt0, qt1, exact, causal, s, ctx->num_sms,
@@ -437,18 +510,20 @@ plsh_status item_table(plsh::DeviceCtx* ctx, int B, int Hq, int Hkv, int QT, int
     t.host = std::move(lst.items);
     t.ext = std::move(lst.ext);
     t.merge = std::move(lst.merge);
+    t.home = st;
     int slots = 0;
     for (size_t k = 1; k < t.merge.size(); k += 2) slots += t.merge[k].y;
-    plsh_status s1 = dev_alloc((void**)&t.dev, sizeof(int4) * t.host.size(), "item table");
+    plsh_status s1 = dev_alloc_async((void**)&t.dev, sizeof(int4) * t.host.size(), st,
+                                     "item table");
     if (s1 == PLSH_OK && !t.ext.empty())
-      s1 = dev_alloc((void**)&t.dev_ext, sizeof(int4) * t.ext.size(), "item table");
+      s1 = dev_alloc_async((void**)&t.dev_ext, sizeof(int4) * t.ext.size(), st, "item table");
     if (s1 == PLSH_OK && !t.merge.empty())
-      s1 = dev_alloc((void**)&t.dev_merge, sizeof(int4) * t.merge.size(), "item table");
+      s1 = dev_alloc_async((void**)&t.dev_merge, sizeof(int4) * t.merge.size(), st, "item table");
     if (s1 == PLSH_OK && slots > 0)
-      s1 = dev_alloc((void**)&t.ws, sizeof(float) * plsh::kSplitSlotFloats * slots,
-                     "split workspace");
+      s1 = dev_alloc_async((void**)&t.ws, sizeof(float) * plsh::kSplitSlotFloats * slots, st,
+                           "split workspace");
     if (s1 != PLSH_OK) {
-      free_table(t);
+      free_table(t, st);
       return s1;
     }
     cudaError_t e = cudaMemcpyAsync(t.dev, t.host.data(), sizeof(int4) * t.host.size(),
@@ -459,11 +534,16 @@ plsh_status item_table(plsh::DeviceCtx* ctx, int B, int Hq, int Hkv, int QT, int
     if (e == cudaSuccess && !t.merge.empty())
       e = cudaMemcpyAsync(t.dev_merge, t.merge.data(), sizeof(int4) * t.merge.size(),
                           cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&t.ready, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventRecord(t.ready, st);
     if (e != cudaSuccess) {
-      free_table(t);
+      free_table(t, st);
       return cuda_fail(e, "item table upload");
     }
     it = ctx->tables.emplace(key, std::move(t)).first;
+  } else if (it->second.home != st && it->second.ready != nullptr) {
+    // another stream built the table: order this call behind its upload
+    PLSH_TRY_CUDA(cudaStreamWaitEvent(st, it->second.ready, 0), "stream wait");
   }
   it->second.last_use = ++ctx->table_clock;
   out->items = it->second.dev;
@@ -472,6 +552,8 @@ plsh_status item_table(plsh::DeviceCtx* ctx, int B, int Hq, int Hkv, int QT, int
   out->merge = it->second.dev_merge;
   out->merges = (int)it->second.merge.size() / 2;
   out->ws = it->second.ws;
+  it->second.pins += 1;
+  out->table = &it->second;
   return PLSH_OK;
 }
 
@@ -556,6 +638,7 @@ plsh_status run_attention(const plsh_tensor* Q, const plsh_tensor* K, const plsh
                                       "path only (bf16, d = 128)");
   a.lse = lse;
   TableRef tab;
+  TableHold hold{&tab, st};
   if (path == Path::Tc) {
     const int QT = (int)((Q->n + 127) / 128);
     plsh_status s1 = item_table(ctx, a.B, a.Hq, a.Hkv, QT, qt0, qt1 < 0 ? QT : qt1, a.exact != 0,
@@ -568,6 +651,7 @@ plsh_status run_attention(const plsh_tensor* Q, const plsh_tensor* K, const plsh
     a.item_ext = tab.ext;
     a.split_ws = tab.ws;
   }
+  hold.used = true;
   cudaError_t e = path == Path::Tc ? plsh::launch_attn_tc(a, slopes, ctx->num_sms, st)
                                    : plsh::launch_attn_simt(a, slopes, Q->dtype, st);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
@@ -864,6 +948,8 @@ plsh_status backward_impl(const plsh_tensor* Q, const plsh_tensor* K, const plsh
     }
     const int QT = (int)((Q->n + 127) / 128);
     TableRef tab;
+    TableHold hold{&tab, cs};
+    hold.used = true;
     plsh_status s1 = item_table(ctx, a.B, a.Hq, a.Hkv, QT, 0, QT, false, a.causal != 0, a.s,
                                 bins->sigma_host, 1, cs, &tab);
     if (s1 == PLSH_OK) {
@@ -1077,14 +1163,17 @@ plsh_status plsh_alibi_attn_host(const plsh_tensor* Q, const plsh_tensor* K,
       for (cudaEvent_t& e : ctx->ev)
         PLSH_TRY_CUDA(cudaEventCreateWithFlags(&e, cudaEventDisableTiming), "event");
     }
+    // this call follows the previous one (its last copy out recorded ev[1];
+    // an event never recorded is no wait): the staging buffers are free
+    // then, and grow in stream order without synchronising the device
+    PLSH_TRY_CUDA(cudaStreamWaitEvent(cs, ctx->ev[1], 0), "stream wait");
     for (int k = 0; k < 4; ++k) {
       if (ctx->stage_bytes[k] >= bytes[k]) continue;
-      // grow (the old buffer may still be in use by earlier calls)
-      PLSH_TRY_CUDA(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
-      cudaFree(ctx->stage[k]);
+      if (ctx->stage[k] != nullptr) PLSH_TRY_CUDA(cudaFreeAsync(ctx->stage[k], cs), "host staging");
       ctx->stage[k] = nullptr;
       ctx->stage_bytes[k] = 0;
-      if ((st = dev_alloc(&ctx->stage[k], bytes[k], "host staging")) != PLSH_OK) return st;
+      if ((st = dev_alloc_async(&ctx->stage[k], bytes[k], cs, "host staging")) != PLSH_OK)
+        return st;
       ctx->stage_bytes[k] = bytes[k];
     }
   }

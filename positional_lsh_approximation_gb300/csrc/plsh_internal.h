@@ -63,6 +63,14 @@ struct ItemTable {
   int4* dev_merge = nullptr;
   float* ws = nullptr;
   uint64_t last_use = 0;
+  // device memory is stream-ordered: allocated and uploaded on `home`
+  // (`ready` recorded behind the upload), freed behind the events that the
+  // calls using it recorded on their streams; `pins` counts the calls between
+  // lookup and launch, which keep the table from being evicted
+  cudaStream_t home = nullptr;
+  cudaEvent_t ready = nullptr;
+  int pins = 0;
+  std::vector<std::pair<cudaStream_t, cudaEvent_t>> uses;
 };
 // floats of one split part's workspace slot: both tiles' rows of P V, then
 // their maxima, then their row sums

@@ -116,6 +116,11 @@ SMALL = [
     ("bf16_s48", 1, 2, 2, 640, 128, "bf16", True, 48, (2.0, 30.0)),
     ("bf16_s64", 1, 2, 2, 640, 128, "bf16", True, 64, (2.0, 30.0)),
     ("bf16_noncausal_s30", 1, 2, 1, 400, 128, "bf16", False, 30, (0.8, 40.0)),
+    # the largest s the tensor-core kernel's shared memory holds (52 with the
+    # causal mask, 29 without), and the next one up (CUDA cores)
+    ("bf16_s52", 1, 2, 1, 520, 128, "bf16", True, 52, (2.0, 30.0)),
+    ("bf16_s53", 1, 2, 1, 300, 128, "bf16", True, 53, (2.0, 30.0)),
+    ("bf16_noncausal_s29", 1, 2, 1, 400, 128, "bf16", False, 29, (0.8, 40.0)),
     # every register-slot variant of the fused kernel (s rounded up to 4, 8,
     # 10, 12 or 16 causal; 8 or 16 without the causal mask)
     ("bf16_s7", 1, 2, 1, 900, 128, "bf16", True, 7, (2.5, 90.0)),
@@ -402,3 +407,26 @@ def test_automatic_split_long_envelopes():
     assert_close(gather_rows(O, rows), ref, "bf16", "automatic split")
     assert_close(gather_rows(O1, rows), ref, "bf16", "unsplit")
     bins.free()
+
+
+def test_item_table_cache_eviction():
+    """More shapes than the item-table cache holds: tables of shapes no call
+    holds are freed in stream order behind their last use, and a shape seen
+    again after its table was evicted gives the same output bit for bit."""
+    d, Hq, Hkv, s = 128, 2, 1, 4
+    outs = {}
+    first = None
+    for k in range(20):
+        n = 256 + 128 * k
+        w = Workload(f"ev{k}", 1, Hq, Hkv, n, d, "bf16", True, s, (3.0, 40.0), qkv_seed=500 + k)
+        Q, K, V = (to_dev(x, "bf16") for x in make_qkv(w))
+        bins = plsh.sample_bins(n, w.sigmas(), s, seed=11)
+        O = plsh.alibi_attn(Q, K, V, bins, True)
+        plsh.stream_status()
+        if k == 0:
+            first = (Q, K, V, bins)
+            outs[k] = O.clone()
+    Q, K, V, bins = first
+    again = plsh.alibi_attn(Q, K, V, bins, True)
+    plsh.stream_status()
+    assert torch.equal(again, outs[0])
