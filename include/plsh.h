@@ -310,7 +310,7 @@ plsh_status plsh_alibi_attn_lse(const plsh_tensor* Q, const plsh_tensor* K,
  * The first call on each device resolves the array's device address
  * (cudaGetSymbolAddress) and keeps it for the life of the device's primary
  * context (a process that resets the device must not call this entry point
- * again); make that first call before any stream capture.
+ * again).
  * Every call on a device shares the one array and each call resets its work
  * counters before use, so calls whose kernels overlap on the GPU (different
  * streams without ordering) race and must not be issued.  A device-side wait
