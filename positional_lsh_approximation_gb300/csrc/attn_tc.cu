@@ -26,7 +26,8 @@
 // one head), sharing every K/V tile:
 //   warp 10     scheduler: pops items from a global queue (cost order),
 //               stages the rows' bin records in shared memory, finds the key
-//               envelope and publishes the item in a three-deep ring;
+//               envelope and publishes the item in a two-deep ring (one
+//               item staged behind the one in progress);
 //   warp 8      producer: TMA-loads the item's first K tile, then Q_A and
 //               Q_B, then the other K/V tiles from the diagonal tile down
 //               (a ring of three 32 KB slots);
