@@ -430,3 +430,23 @@ def test_item_table_cache_eviction():
     again = plsh.alibi_attn(Q, K, V, bins, True)
     plsh.stream_status()
     assert torch.equal(again, outs[0])
+
+
+def test_item_table_built_on_another_stream():
+    """A shape's first call on one stream builds its item table there; a call
+    of the same shape queued at once on a second stream (no host
+    synchronisation between them) waits for that upload by event and gives
+    the same output bit for bit."""
+    n, d, s = 1664, 128, 6
+    w = Workload("xs", 1, 2, 1, n, d, "bf16", True, s, (2.0, 70.0), qkv_seed=77)
+    Q, K, V = (to_dev(x, "bf16") for x in make_qkv(w))
+    bins = plsh.sample_bins(n, w.sigmas(), s, seed=5)
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    O1 = torch.empty_like(Q)
+    O2 = torch.empty_like(Q)
+    plsh.alibi_attn(Q, K, V, bins, True, out=O1, stream=s1)
+    plsh.alibi_attn(Q, K, V, bins, True, out=O2, stream=s2)
+    torch.cuda.synchronize()
+    plsh.stream_status()
+    assert torch.equal(O1, O2)
