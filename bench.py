@@ -158,6 +158,18 @@ def kernel_traffic():
 KERNEL_SOURCES = ("attn_tc.cu", "tc_ptx.cuh", "bins_dev.cuh", "plsh_internal.h")
 
 
+def workload_config(w, world: int) -> dict:
+    """The bench line's `config`: the workload and the timing protocol of the
+    GPU arm; the oracle arm reports the same object, so that the two lines
+    name one configuration."""
+    return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "n": w.n,
+            "d": w.d, "s": w.s, "causal": w.causal,
+            "sigma": "ALiBi slopes sigma_h = 2^(8h/H)" if not w.sigma else list(w.sigma),
+            "hashes": "redrawn on the device every step (same seed)",
+            "l2": "flushed between timed steps (256 MiB write)",
+            "parallelism": f"replicas x{world}"}
+
+
 def kernel_source_digest() -> str:
     """sha256 (16 hex digits) over the fused kernel's source files."""
     h = hashlib.sha256()
@@ -332,12 +344,7 @@ def run_ours(args, rank, world):
         "vs_baseline": None,
         "dtype": "bf16" if w.dtype == "bf16" else "f32",
         "data": "synthetic (seeded N(0,1) Q/K/V of the workload's shape, no weights)",
-        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "n": w.n,
-                   "d": w.d, "s": w.s, "causal": w.causal,
-                   "sigma": "ALiBi slopes sigma_h = 2^(8h/H)" if not w.sigma else list(w.sigma),
-                   "hashes": "redrawn on the device every step (same seed)",
-                   "l2": "flushed between timed steps (256 MiB write)",
-                   "parallelism": f"replicas x{world}"},
+        "config": workload_config(w, world),
         "roofline": {
             "bound": "tensor",
             "achieved": achieved_tf,
@@ -779,8 +786,7 @@ def run_reference(args, rank, world):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic (seeded N(0,1) Q/K/V of the workload's shape, no weights)",
-        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "n": w.n,
-                   "d": w.d, "s": w.s, "causal": w.causal},
+        "config": workload_config(w, world),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "kind": "oracle",
                          "cores": oracle.max_threads(), "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
