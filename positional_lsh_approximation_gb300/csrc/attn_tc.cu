@@ -1486,6 +1486,11 @@ bool make_tile_map_bf16(CUtensorMap* map, const void* base, int64_t planes, int6
   return make_map(map, base, planes, n, BM, HD);
 }
 
+bool make_rows_map_bf16(CUtensorMap* map, const void* base, int64_t planes, int64_t n,
+                        int box_rows, int d) {
+  return make_map(map, base, planes, n, box_rows, d);
+}
+
 size_t attn_tc_smem_bytes(int s, int causal, int exact) {
   return smem_for(kSlots, out_staged(s, causal, exact), s, causal, exact);
 }

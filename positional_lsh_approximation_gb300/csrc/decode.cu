@@ -16,17 +16,21 @@
 // is split over the envelope, flash-decoding style, so that the GPU holds
 // about three CTAs per SM).  The group's key and value rows of a block (16 KB
 // of each) arrive in shared memory by bulk asynchronous copies, double
-// buffered, completing on an mbarrier with a bounded wait (a copy per key row
-// into rows padded by 16 bytes, one copy for the value rows); every head of
-// the group then reads them from shared memory: scores with a key per lane
-// (the padding puts the same 16-byte chunk of consecutive rows in different
-// banks, and every lane reads the same chunk of the query), an online softmax
-// per head, P V with a slice of every row per lane.  Each (batch element, head, share) writes its max m, row
+// buffered, completing on an mbarrier with a bounded wait: in bf16 the key
+// rows as one or two tensor-map tiles (128-byte rows of the tile, 128-byte
+// swizzle: chunk c of row r lands at chunk c ^ (r & 7)), in fp32 a copy per
+// key row into rows padded by 16 bytes, and one copy for the value rows.
+// Every head of the group then reads them from shared memory: scores with a
+// key per lane (the swizzle, or the padding, puts the same 16-byte chunk of
+// consecutive rows in different banks, and every lane reads the same chunk
+// of the query), an online softmax per head, P V with a slice of every row
+// per lane.  Each (batch element, head, share) writes its max m, row
 // sum l and unnormalised P V; a second kernel merges the shares into
 // O = P V / l.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <string.h>
 
 #include "bins_dev.cuh"
 #include "plsh_internal.h"
@@ -90,16 +94,32 @@ struct Cfg {
   static constexpr int kChunks = kRowBytes / 16;               // 16-byte chunks of a row
   static constexpr int kE = 16 / (int)sizeof(T);               // values per chunk
   static constexpr int kPV = D / 32;                           // values of a row per lane
-  static constexpr int kKStride = kRowBytes + 16;              // padded key row
+  // bf16 keys by tensor-map tiles of 64 values x kKeys rows, swizzled; fp32
+  // keys row by row into padded rows
+  static constexpr bool kTiled = sizeof(T) == 2;
+  static constexpr int kBoxes = kTiled ? kRowBytes / 128 : 0;  // tiles per block
+  static_assert(!kTiled || (kBoxes >= 1 && kKeys <= 256), "a tile is 128 bytes x kKeys rows");
+  static constexpr int kKStride = kTiled ? kRowBytes : kRowBytes + 16;
   static constexpr uint32_t kKStage = (uint32_t)(kKeys * kKStride);
-  static constexpr uint32_t kSmem = 2u * kKStage + 2u * kStageBytes;  // K, V x two stages
+  // K, V x two stages, and room to align the swizzled K stages to 1024 bytes
+  static constexpr uint32_t kSmem = 2u * kKStage + 2u * kStageBytes + (kTiled ? 1024u : 0u);
+  // byte offset of chunk k of key row r in a K stage
+  __device__ static uint32_t koff(int r, int k) {
+    if constexpr (kTiled)
+      return (uint32_t)((k >> 3) * (kKeys * 128) + r * 128 + (((k & 7) ^ (r & 7)) << 4));
+    else
+      return (uint32_t)(r * kKStride + k * 16);
+  }
 };
 
 template <typename T, int D>
 __global__ void __launch_bounds__(256)
-decode_group_kernel(DecodeParams p) {
+decode_group_kernel(const __grid_constant__ CUtensorMap tmK, DecodeParams p) {
   using C = Cfg<T, D>;
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw;
+  if constexpr (C::kTiled)
+    smem += (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;   // swizzle atoms: 1 KB
   __shared__ float qs_all[8][D];
   __shared__ float ps_all[8][C::kKeys];
   __shared__ int los_all[8][kMaxS];
@@ -162,14 +182,26 @@ decode_group_kernel(DecodeParams p) {
     const uint32_t bytes = (uint32_t)(cnt * C::kRowBytes);
     const uint32_t st = (uint32_t)(blk & 1);
     const uint32_t fb = smem_u32(&full[st]);
-    if (lane == 0) {
-      mbar_arrive_expect_tx(fb, 2 * bytes);
-      bulk_load(sV + st * kStageBytes, Vg + (int64_t)j0 * C::kRowBytes, bytes, fb);
+    if constexpr (C::kTiled) {
+      // whole tiles (rows past the block are loaded too; past n, zeros)
+      if (lane == 0) {
+        mbar_arrive_expect_tx(fb, bytes + (uint32_t)(C::kBoxes * C::kKeys * 128));
+        bulk_load(sV + st * kStageBytes, Vg + (int64_t)j0 * C::kRowBytes, bytes, fb);
+#pragma unroll
+        for (int x = 0; x < C::kBoxes; ++x)
+          tma_load_3d(sK + st * C::kKStage + (uint32_t)(x * C::kKeys * 128), &tmK, fb, 64 * x,
+                      j0, b * p.Hkv + g);
+      }
+    } else {
+      if (lane == 0) {
+        mbar_arrive_expect_tx(fb, 2 * bytes);
+        bulk_load(sV + st * kStageBytes, Vg + (int64_t)j0 * C::kRowBytes, bytes, fb);
+      }
+      __syncwarp();
+      for (int r = lane; r < cnt; r += 32)
+        bulk_load(sK + st * C::kKStage + (uint32_t)r * C::kKStride,
+                  Kg + (int64_t)(j0 + r) * C::kRowBytes, C::kRowBytes, fb);
     }
-    __syncwarp();
-    for (int r = lane; r < cnt; r += 32)
-      bulk_load(sK + st * C::kKStage + (uint32_t)r * C::kKStride,
-                Kg + (int64_t)(j0 + r) * C::kRowBytes, C::kRowBytes, fb);
   };
   int issued = 0;
   if (warp == 0) {
@@ -205,11 +237,10 @@ decode_group_kernel(DecodeParams p) {
           int c = 0;
           for (int t = 0; t < p.s; ++t) c += los[t] <= j ? 1 : 0;
           if (c > 0) {
-            const uint32_t krow = kst + (uint32_t)jj * C::kKStride;
             float a0 = 0.f, a1 = 0.f;
 #pragma unroll 4
             for (int k = 0; k < C::kChunks; ++k) {
-              const uint4 kv = ld_shared_v4(krow + (uint32_t)k * 16u);
+              const uint4 kv = ld_shared_v4(kst + C::koff(jj, k));
               const float* qq = qs + k * C::kE;
               if constexpr (sizeof(T) == 2) {
                 a0 = fmaf(qq[0], lo16(kv.x), a0);
@@ -329,8 +360,13 @@ cudaError_t launch_typed(const DecodeParams& p, void* out, cudaStream_t st) {
   auto kern = decode_group_kernel<T, D>;
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), (int)C::kSmem);
   if (e != cudaSuccess) return e;
+  // K as [B * Hkv planes, n rows, D] in tiles of 64 values x kKeys rows (bf16)
+  CUtensorMap mk;
+  memset(&mk, 0, sizeof mk);
+  if (C::kTiled && !make_rows_map_bf16(&mk, p.K, (int64_t)p.B * p.Hkv, p.n, C::kKeys, D))
+    return cudaErrorInvalidValue;
   const int64_t ctas = (int64_t)p.B * p.Hkv * p.hchunks * p.splits;
-  kern<<<(unsigned)ctas, 32 * p.heads, C::kSmem, st>>>(p);
+  kern<<<(unsigned)ctas, 32 * p.heads, C::kSmem, st>>>(mk, p);
   decode_merge_kernel<T, D><<<(unsigned)(p.B * p.Hq), D, 0, st>>>(p, out);
   return cudaGetLastError();
 }

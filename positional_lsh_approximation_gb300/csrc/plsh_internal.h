@@ -226,6 +226,10 @@ size_t attn_tc_smem_bytes(int s, int causal, int exact);
 // [planes, n, 128] bf16 as a TMA tensor map with 64 x 128 x 1 boxes, 128-byte
 // swizzle, rows past n reading as zeros (attn_tc.cu)
 bool make_tile_map_bf16(CUtensorMap* map, const void* base, int64_t planes, int64_t n);
+// [planes, n, d] bf16 (d = 64 or 128) as a 3-D tensor map of 64-value x
+// box_rows x 1 tiles with 128-byte swizzle (rows past n read as zeros)
+bool make_rows_map_bf16(CUtensorMap* map, const void* base, int64_t planes, int64_t n,
+                        int box_rows, int d);
 
 // bwd_tc.cu: gradients on the tensor cores (bf16, d = 128, s <= 16) from the
 // rows' statistics [B * Hq * n][2] (-lse, Delta); dq_acc is fp32 scratch of
