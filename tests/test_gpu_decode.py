@@ -70,6 +70,10 @@ CASES = [
     # CTAs per group: eight heads and four)
     ("bf16_g3", 2, 3, 1, 900, 128, "bf16", 4, (5.0, 60.0, 500.0), [899, 450, 63, 64]),
     ("bf16_g12", 1, 24, 2, 700, 128, "bf16", 5, (), [699, 100]),
+    # grids of at least four CTAs per SM take the 8 KB stages (d = 128: 32
+    # keys a block; d = 64: 64)
+    ("bf16_many", 24, 8, 8, 1200, 128, "bf16", 10, (), [1199, 600]),
+    ("bf16_d64_many", 32, 8, 4, 900, 64, "bf16", 6, (), [899, 64]),
 ]
 
 
