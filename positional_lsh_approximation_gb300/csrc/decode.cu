@@ -342,6 +342,9 @@ decode_group_kernel(const __grid_constant__ CUtensorMap tmK, DecodeParams p) {
 template <typename T, int D>
 __global__ void __launch_bounds__(D)
 decode_merge_kernel(DecodeParams p, void* out) {
+  // launched as a programmatic dependent of the group kernel: its launch
+  // overlaps that kernel's tail, and it reads the partials once it is done
+  grid_dep_wait();
   const int bh = blockIdx.x, e = threadIdx.x;
   const int64_t first = (int64_t)bh * p.splits;
   float m = -INFINITY;
@@ -370,7 +373,19 @@ cudaError_t launch_staged(const DecodeParams& p, void* out, cudaStream_t st) {
     return cudaErrorInvalidValue;
   const int64_t ctas = (int64_t)p.B * p.Hkv * p.hchunks * p.splits;
   kern<<<(unsigned)ctas, 32 * p.heads, C::kSmem, st>>>(mk, p);
-  decode_merge_kernel<T, D><<<(unsigned)(p.B * p.Hq), D, 0, st>>>(p, out);
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(p.B * p.Hq));
+    cfg.blockDim = dim3(D);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e2 = cudaLaunchKernelEx(&cfg, decode_merge_kernel<T, D>, p, out);
+    if (e2 != cudaSuccess) return e2;
+  }
   return cudaGetLastError();
 }
 
