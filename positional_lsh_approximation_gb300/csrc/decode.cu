@@ -129,6 +129,9 @@ decode_group_kernel(const __grid_constant__ CUtensorMap tmK, DecodeParams p) {
   __shared__ int lo_warp[8];
   __shared__ __align__(8) uint64_t full[2];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // a programmatic dependent of the kernel before it: nothing in global
+  // memory is read before that kernel has completed
+  grid_dep_wait();
   const int G = p.Hq / p.Hkv;
   int cta = blockIdx.x;
   const int split = cta % p.splits;
@@ -372,7 +375,20 @@ cudaError_t launch_staged(const DecodeParams& p, void* out, cudaStream_t st) {
   if (C::kTiled && !make_rows_map_bf16(&mk, p.K, (int64_t)p.B * p.Hkv, p.n, C::kKeys, D))
     return cudaErrorInvalidValue;
   const int64_t ctas = (int64_t)p.B * p.Hkv * p.hchunks * p.splits;
-  kern<<<(unsigned)ctas, 32 * p.heads, C::kSmem, st>>>(mk, p);
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ctas);
+    cfg.blockDim = dim3(32 * p.heads);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, mk, p);
+    if (e != cudaSuccess) return e;
+  }
   {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(p.B * p.Hq));
