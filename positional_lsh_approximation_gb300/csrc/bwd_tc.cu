@@ -888,6 +888,7 @@ __global__ void __launch_bounds__(256)
 bwd_delta_kernel(const uint2* __restrict__ O, const uint2* __restrict__ dO,
                  const float* __restrict__ lse, float2* __restrict__ stats,
                  float4* __restrict__ acc, int64_t rows) {
+  grid_dep_wait();   // launched as a programmatic dependent: O, dO, lse ready
   const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
@@ -904,6 +905,7 @@ bwd_delta_kernel(const uint2* __restrict__ O, const uint2* __restrict__ dO,
 // dQ = dq_acc / sqrt(128) in bf16
 __global__ void dq_convert_kernel(const float4* __restrict__ acc, uint2* __restrict__ out,
                                   int64_t count4) {
+  grid_dep_wait();   // launched as a programmatic dependent of the backward kernel
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= count4) return;
   const float4 v = acc[i];
@@ -938,6 +940,25 @@ bool make_acc_map(CUtensorMap* map, float* base, int64_t planes, int64_t n) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Launches `kern` as a programmatic dependent of the kernel before it on `st`
+// (each of these kernels waits for that kernel before it touches global
+// memory), so that its launch overlaps that kernel's tail.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                             cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 }  // namespace
 
 size_t bwd_tc_smem_bytes() { return 1024 + OFF_END + sizeof(CtlB); }
@@ -945,10 +966,10 @@ size_t bwd_tc_smem_bytes() { return 1024 + OFF_END + sizeof(CtlB); }
 cudaError_t launch_bwd_delta(const void* O, const void* dO, const float* lse, float* stats,
                              float* dq_acc, int64_t rows, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
-  bwd_delta_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(
-      static_cast<const uint2*>(O), static_cast<const uint2*>(dO), lse,
-      reinterpret_cast<float2*>(stats), reinterpret_cast<float4*>(dq_acc), rows);
-  return cudaGetLastError();
+  return launch_dependent(bwd_delta_kernel, (unsigned)((rows + 7) / 8), 256, 0, st,
+                          static_cast<const uint2*>(O), static_cast<const uint2*>(dO), lse,
+                          reinterpret_cast<float2*>(stats), reinterpret_cast<float4*>(dq_acc),
+                          rows);
 }
 
 cudaError_t launch_attn_bwd_tc(const void* Q, const void* K, const void* V, const void* dO,
@@ -1011,13 +1032,12 @@ cudaError_t launch_attn_bwd_tc(const void* Q, const void* K, const void* V, cons
   e = set_smem_limit(reinterpret_cast<const void*>(kern), (int)smem);
   if (e != cudaSuccess) return e;
   const int grid = p.num_items < num_sms ? p.num_items : num_sms;
-  kern<<<grid, kThreads, smem, st>>>(mq, mk, mv, mdo, macc, p);
-  e = cudaGetLastError();
+  e = launch_dependent(kern, (unsigned)grid, kThreads, smem, st, mq, mk, mv, mdo, macc, p);
   if (e != cudaSuccess) return e;
   const int64_t count4 = (int64_t)B * Hq * n * HD / 4;
-  dq_convert_kernel<<<(unsigned)((count4 + 255) / 256), 256, 0, st>>>(
-      reinterpret_cast<const float4*>(dq_acc), static_cast<uint2*>(dQ), count4);
-  return cudaGetLastError();
+  return launch_dependent(dq_convert_kernel, (unsigned)((count4 + 255) / 256), 256, 0, st,
+                          reinterpret_cast<const float4*>(dq_acc), static_cast<uint2*>(dQ),
+                          count4);
 }
 
 }  // namespace plsh
