@@ -1296,6 +1296,7 @@ plsh_status plsh_alibi_decode(const plsh_tensor* q, const plsh_tensor* K, const 
   a.dtype = q->dtype;
   a.num_sms = ctx->num_sms;
   a.useful_splits = useful;
+  a.sigma = (int64_t)bins->sigma_host.size() == q->H ? bins->sigma_host.data() : nullptr;
   a.work = work;
   a.err = ctx->d_err;
   a.wait_ns = ctx->wait_ns;

@@ -46,6 +46,7 @@ using namespace ptx;
 constexpr int kStageBytes = 16384;
 constexpr int kSmallStageBytes = 8192;
 constexpr unsigned FULL = 0xffffffffu;
+constexpr int kMaxGroupOrder = 64;
 
 // 1-D bulk copy global -> shared memory, completion counted in bytes on an
 // mbarrier of this CTA (both addresses 16-byte aligned, size a multiple of 16)
@@ -83,6 +84,8 @@ struct DecodeParams {
   int heads;            // query heads per CTA (<= 8)
   int hchunks;          // CTAs per KV group and share
   int splits;           // shares of the envelope
+  int g_order[kMaxGroupOrder];   // KV groups, widest expected envelope first
+  int ordered;          // 0: groups in index order (more than kMaxGroupOrder)
   float* part_m;        // [B * Hq * splits]
   float* part_l;
   float* part_o;        // [B * Hq * splits][D]
@@ -138,7 +141,11 @@ decode_group_kernel(const __grid_constant__ CUtensorMap tmK, DecodeParams p) {
   cta /= p.splits;
   const int hc = cta % p.hchunks;
   cta /= p.hchunks;
-  const int g = cta % p.Hkv, b = cta / p.Hkv;
+  // KV groups with the widest expected envelopes first (the CTAs with the
+  // most blocks start in the first wave), every batch element of a group
+  // together
+  const int b = cta % p.B, gr = cta / p.B;
+  const int g = p.ordered ? p.g_order[gr] : gr;
   const int hg = hc * p.heads + warp;                // head within the group
   const bool valid = hg < G;
   const int h = g * G + (valid ? hg : 0);
@@ -435,6 +442,25 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
   p.heads = decode_heads(a.Hq / a.Hkv);
   p.hchunks = (a.Hq / a.Hkv + p.heads - 1) / p.heads;
   p.splits = decode_splits(a.B, a.Hq, a.Hkv, a.num_sms, a.useful_splits);
+  // the envelope of a group reaches about its widest scale back: groups by
+  // their largest sigma, descending (stable)
+  p.ordered = 0;
+  if (a.sigma != nullptr && a.Hkv <= kMaxGroupOrder) {
+    const int G = a.Hq / a.Hkv;
+    double key[kMaxGroupOrder];
+    for (int g = 0; g < a.Hkv; ++g) {
+      key[g] = 0.0;
+      for (int h = g * G; h < (g + 1) * G; ++h) key[g] = a.sigma[h] > key[g] ? a.sigma[h] : key[g];
+      p.g_order[g] = g;
+    }
+    for (int i = 1; i < a.Hkv; ++i)        // insertion sort, stable
+      for (int j = i; j > 0 && key[p.g_order[j]] > key[p.g_order[j - 1]]; --j) {
+        const int t = p.g_order[j];
+        p.g_order[j] = p.g_order[j - 1];
+        p.g_order[j - 1] = t;
+      }
+    p.ordered = 1;
+  }
   p.part_m = a.work;
   p.part_l = a.work + (size_t)a.B * a.Hq * p.splits;
   p.part_o = a.work + 2 * (size_t)a.B * a.Hq * p.splits;

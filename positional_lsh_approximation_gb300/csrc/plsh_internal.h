@@ -205,6 +205,7 @@ struct DecodeArgs {
   int dtype;             // PLSH_BF16 or PLSH_F32
   int num_sms;
   int useful_splits;     // decode_useful_splits of the widest bins
+  const double* sigma;   // host [Hq] scales of the heads' bins, or null if unknown
   float* work;           // decode_work_floats(B, Hq, Hkv, d, num_sms, useful_splits)
   int* err;              // device error flag (bit 0: a bounded wait ran out)
   uint64_t wait_ns;
