@@ -46,7 +46,7 @@ using namespace ptx;
 constexpr int kStageBytes = 16384;
 constexpr int kSmallStageBytes = 8192;
 constexpr unsigned FULL = 0xffffffffu;
-constexpr int kMaxGroupOrder = 64;
+constexpr int kMaxGroupOrder = 32;   // more KV groups: index order, uniform shares
 
 // 1-D bulk copy global -> shared memory, completion counted in bytes on an
 // mbarrier of this CTA (both addresses 16-byte aligned, size a multiple of 16)
@@ -84,8 +84,12 @@ struct DecodeParams {
   int heads;            // query heads per CTA (<= 8)
   int hchunks;          // CTAs per KV group and share
   int splits;           // shares of the envelope
-  int g_order[kMaxGroupOrder];   // KV groups, widest expected envelope first
-  int ordered;          // 0: groups in index order (more than kMaxGroupOrder)
+  // (kept small: the parameters are copied at every launch)
+  uint8_t g_order[kMaxGroupOrder];    // KV groups, widest expected envelope first
+  uint8_t g_shares[kMaxGroupOrder];   // shares of each group in that order (<= splits)
+  uint8_t shares_of[kMaxGroupOrder];  // shares of group g (index order)
+  int g_first[kMaxGroupOrder + 1];    // first CTA of each group in order; [Hkv]: the grid
+  int ordered;          // 0: groups in index order, `splits` shares each
   float* part_m;        // [B * Hq * splits]
   float* part_l;
   float* part_o;        // [B * Hq * splits][D]
@@ -136,15 +140,21 @@ decode_group_kernel(const __grid_constant__ CUtensorMap tmK, DecodeParams p) {
   // memory is read before that kernel has completed
   grid_dep_wait();
   const int G = p.Hq / p.Hkv;
-  int cta = blockIdx.x;
-  const int split = cta % p.splits;
-  cta /= p.splits;
-  const int hc = cta % p.hchunks;
-  cta /= p.hchunks;
   // KV groups with the widest expected envelopes first (the CTAs with the
   // most blocks start in the first wave), every batch element of a group
-  // together
-  const int b = cta % p.B, gr = cta / p.B;
+  // together, each group cut into as many shares as its own envelope wants
+  int cta = blockIdx.x, S = p.splits, gr = 0;
+  if (p.ordered) {
+    while (gr + 1 < p.Hkv && cta >= p.g_first[gr + 1]) ++gr;
+    cta -= p.g_first[gr];
+    S = p.g_shares[gr];
+  }
+  const int split = cta % S;
+  cta /= S;
+  const int hc = cta % p.hchunks;
+  cta /= p.hchunks;
+  const int b = cta % p.B;
+  if (!p.ordered) gr = cta / p.B;
   const int g = p.ordered ? p.g_order[gr] : gr;
   const int hg = hc * p.heads + warp;                // head within the group
   const bool valid = hg < G;
@@ -178,7 +188,7 @@ decode_group_kernel(const __grid_constant__ CUtensorMap tmK, DecodeParams p) {
   int lo_cta = p.pos;
   for (int w = 0; w < p.heads; ++w) lo_cta = min(lo_cta, lo_warp[w]);
   const int env = p.pos - lo_cta + 1;
-  const int len = (env + p.splits - 1) / p.splits;
+  const int len = (env + S - 1) / S;
   const int j_begin = lo_cta + split * len;
   const int j_end = min(p.pos + 1, j_begin + len);
   const int nblk = j_begin < j_end ? (j_end - j_begin + C::kKeys - 1) / C::kKeys : 0;
@@ -357,11 +367,12 @@ decode_merge_kernel(DecodeParams p, void* out) {
   grid_dep_wait();
   const int bh = blockIdx.x, e = threadIdx.x;
   const int64_t first = (int64_t)bh * p.splits;
+  const int S = p.ordered ? p.shares_of[(bh % p.Hq) / (p.Hq / p.Hkv)] : p.splits;
   float m = -INFINITY;
-  for (int k = 0; k < p.splits; ++k)
+  for (int k = 0; k < S; ++k)
     if (p.part_l[first + k] > 0.f) m = fmaxf(m, p.part_m[first + k]);
   float l = 0.f, o = 0.f;
-  for (int k = 0; k < p.splits; ++k) {
+  for (int k = 0; k < S; ++k) {
     if (!(p.part_l[first + k] > 0.f)) continue;
     const float f = exp2f(p.part_m[first + k] - m);
     l = fmaf(f, p.part_l[first + k], l);
@@ -381,7 +392,8 @@ cudaError_t launch_staged(const DecodeParams& p, void* out, cudaStream_t st) {
   memset(&mk, 0, sizeof mk);
   if (C::kTiled && !make_rows_map_bf16(&mk, p.K, (int64_t)p.B * p.Hkv, p.n, C::kKeys, D))
     return cudaErrorInvalidValue;
-  const int64_t ctas = (int64_t)p.B * p.Hkv * p.hchunks * p.splits;
+  const int64_t ctas =
+      p.ordered ? p.g_first[p.Hkv] : (int64_t)p.B * p.Hkv * p.hchunks * p.splits;
   {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)ctas);
@@ -418,7 +430,8 @@ cudaError_t launch_staged(const DecodeParams& p, void* out, cudaStream_t st) {
 template <typename T, int D>
 cudaError_t launch_typed(const DecodeParams& p, void* out, int num_sms, cudaStream_t st) {
   if constexpr (sizeof(T) == 2) {
-    const int64_t ctas = (int64_t)p.B * p.Hkv * p.hchunks * p.splits;
+    const int64_t ctas =
+        p.ordered ? p.g_first[p.Hkv] : (int64_t)p.B * p.Hkv * p.hchunks * p.splits;
     if (ctas >= 4LL * num_sms) return launch_staged<T, D, kSmallStageBytes>(p, out, st);
   }
   return launch_staged<T, D, kStageBytes>(p, out, st);
@@ -451,14 +464,37 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
     for (int g = 0; g < a.Hkv; ++g) {
       key[g] = 0.0;
       for (int h = g * G; h < (g + 1) * G; ++h) key[g] = a.sigma[h] > key[g] ? a.sigma[h] : key[g];
-      p.g_order[g] = g;
+      p.g_order[g] = (uint8_t)g;
     }
     for (int i = 1; i < a.Hkv; ++i)        // insertion sort, stable
       for (int j = i; j > 0 && key[p.g_order[j]] > key[p.g_order[j - 1]]; --j) {
-        const int t = p.g_order[j];
+        const uint8_t t = p.g_order[j];
         p.g_order[j] = p.g_order[j - 1];
         p.g_order[j - 1] = t;
       }
+    // a grid of eight or more CTAs per SM: each group cut into shares of
+    // about 64 keys of its own expected envelope (about 1.2 sigma + 32 keys;
+    // at most `splits`, the call's share count, which sized the partials),
+    // so that narrow groups do not spread a few keys over many CTAs; smaller
+    // grids keep `splits` shares for every group (more CTAs run in parallel
+    // there).  Measured on the Mistral shape: 32 and 64 sequences 20.1 ->
+    // 17.5 and 24.8 -> 23.0 us back to back; at 1, 8 and 16 sequences the
+    // per-group shares were slower.
+    const bool per_group =
+        (int64_t)a.B * a.Hkv * p.hchunks * p.splits >= 8LL * a.num_sms;
+    int64_t first = 0;
+    for (int gr = 0; gr < a.Hkv; ++gr) {
+      const int g = p.g_order[gr];
+      const double keys = 1.2 * key[g] + 32.0;
+      const double lim = a.pos + 1.0 < keys ? a.pos + 1.0 : keys;
+      const int want = per_group ? (int)(lim / 64.0 + 1.0) : p.splits;
+      const int sh = want < 1 ? 1 : (want > p.splits ? p.splits : want);
+      p.g_shares[gr] = (uint8_t)sh;
+      p.shares_of[g] = (uint8_t)sh;
+      p.g_first[gr] = (int)first;
+      first += (int64_t)a.B * p.hchunks * sh;
+    }
+    p.g_first[a.Hkv] = (int)first;
     p.ordered = 1;
   }
   p.part_m = a.work;
