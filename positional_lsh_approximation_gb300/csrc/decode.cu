@@ -13,9 +13,11 @@
 //
 // A CTA serves the query heads of one KV group (up to eight, a warp each) of
 // one batch element, over a share of the union of their envelopes (the work
-// is split over the envelope, flash-decoding style, so that the GPU holds
-// about three CTAs per SM).  The group's key and value rows of a block (16 KB
-// of each) arrive in shared memory by bulk asynchronous copies, double
+// is split over the envelope, flash-decoding style, into about twelve CTAs
+// per SM in all; on large grids each group takes as many shares as its own
+// expected envelope wants; the groups with the widest scales come first in
+// the grid).  The group's key and value rows of a block (16 KB of each, 8 KB
+// on large bf16 grids) arrive in shared memory by bulk asynchronous copies, double
 // buffered, completing on an mbarrier with a bounded wait: in bf16 the key
 // rows as one or two tensor-map tiles (128-byte rows of the tile, 128-byte
 // swizzle: chunk c of row r lands at chunk c ^ (r & 7)), in fp32 a copy per
