@@ -389,7 +389,10 @@ plsh_status plsh_alibi_exact(const plsh_tensor* Q, const plsh_tensor* K,
  * chosen so that about 12 CTAs per SM run, at most the 64-key shares of the
  * envelope the widest bins are expected to reach; grown on demand in stream
  * order on `stream`; calls on different streams are ordered on it by an
- * event).
+ * event).  Up to 32 KV groups are listed widest scale first, and on large
+ * grids each group takes the shares its own expected envelope wants.  Both
+ * kernels of a call start as programmatic dependents of the kernel before
+ * them on `stream` (neither touches global memory before it completes).
  * Asynchronous on `stream`; errors in the arguments return before any launch.
  */
 plsh_status plsh_alibi_decode(const plsh_tensor* q, const plsh_tensor* K,
